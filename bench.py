@@ -1,0 +1,551 @@
+#!/usr/bin/env python3
+"""Benchmark of one continuous-batching attention step over a paged KV cache.
+
+Headline (`value`): query tokens/s of the mixed step -- 8 chunked-prefill
+chunks of 512 tokens (cached context uniform in 0..8192), 192 decode rows
+(seq_len uniform in 256..8192) and 32 speculative-verify rows of 1+4 tokens;
+32 q / 8 kv heads, head_dim 128, block_size 16, bf16.  One step = write the
+4448 new K/V rows through the slot mapping + attention for every row (device
+planner, split-KV kernel, tensor-core kernel, fused split merge).  Inputs are
+resident in HBM and larger than L2 (about 3.9 GB of KV is read per step), so
+no L2 flush is needed between steps.
+
+Also reported on the same line:
+  roofline      the split-KV kernel (the step's largest share of time):
+                algorithmic bytes per launch / its CUDA-event duration inside
+                the timed region, against the measured HBM copy bandwidth;
+  tensor_core   the same for the tcgen05 prefill kernel in TFLOP/s;
+  decode_heavy  256 decode rows, seq_len uniform in 512..4096: KV GB/s;
+  cascade       64 requests sharing an 8192-token prefix: cascade decode vs
+                plain paged attention over the full tables;
+  e2e           the same step through the public API with host buffers
+                (pinned host -> device copies of the step's inputs and
+                device -> host copy of out/lse inside the timed region);
+  cpu_baseline  the fp64 CPU oracle on a 1/8 sample of the step.
+
+`--impl reference` times the CPU oracle itself (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "decode paged-attn KV GB/s (% HBM peak); mixed-step query tokens/s on 1 GB300"
+WORKLOAD = ("mixed continuous-batching step: 8 chunked-prefill chunks x 512 tokens "
+            "(context U[0,8192]) + 192 decode rows (seq_len U[256,8192]) + 32 spec-verify "
+            "rows of 1+4 tokens; 32 q / 8 kv heads, d=128, block_size 16, bf16")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---------------------------------------------------------------------------
+# environment
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(
+            p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# workloads on the device
+# ---------------------------------------------------------------------------
+
+class DeviceStep:
+    def __init__(self, pool, step, dev, seed_note=""):
+        import paged_kv_cache_284_gb300 as pk
+        self.pk = pk
+        self.step = step
+        self.dev = dev
+        self.kc = pool.k_cache.to(dev)
+        self.vc = pool.v_cache.to(dev)
+        self.q = step.q.to(dev)
+        self.k = step.k.to(dev)
+        self.v = step.v.to(dev)
+        self.slots = step.slot_mapping.to(dev)
+        self.bt = step.block_tables.to(dev)
+        self.qsl = step.query_start_loc.to(dev)
+        self.ctx = step.context_lens.to(dev)
+        self.sl = step.seq_lens.to(dev)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=dev)
+        T, hq, d = self.q.shape
+        self.ws = pk.alloc_workspace(pk.workspace_size(step.num_seqs, T, hq, step.num_kv_heads, d),
+                                     dev)
+
+    def run(self, write=True):
+        pk = self.pk
+        if write:
+            pk.pa_write_kv(self.k, self.v, self.slots, self.kc, self.vc)
+        pk.pa_attention(self.q, self.kc, self.vc, self.bt, self.qsl, self.ctx, self.sl,
+                        self.step.scale, self.out, self.lse, workspace=self.ws)
+
+
+def split_rows(step, short_max_rows=64):
+    """Indices of requests the split-KV kernel takes (q_len*group <= 64)."""
+    g = step.num_q_heads // step.num_kv_heads
+    ql = step.q_lens.tolist()
+    return [b for b, n in enumerate(ql) if 0 < n * g <= short_max_rows]
+
+
+def algorithmic_bytes(step, reqs):
+    """HBM bytes a perfect kernel must move for these requests: each visible
+    K and V row once per kv head, q read once, out + lse written once, and
+    the block-table entries (per kv head)."""
+    hkv, hq, d, bs = step.num_kv_heads, step.num_q_heads, step.head_dim, step.block_size
+    total = 0
+    for b in reqs:
+        L = int(step.seq_lens[b])
+        n = int(step.query_start_loc[b + 1] - step.query_start_loc[b])
+        total += 2 * L * hkv * d * 2            # K and V
+        total += 2 * n * hq * d * 2 + n * hq * 4  # q, out, lse
+        total += math.ceil(L / bs) * 4 * hkv     # block table
+    return total
+
+
+def kv_bytes(step, reqs):
+    hkv, d = step.num_kv_heads, step.head_dim
+    return sum(2 * int(step.seq_lens[b]) * hkv * d * 2 for b in reqs)
+
+
+def tensor_core_flops(step, reqs):
+    """4 * d * Hq flops per visible (query, key) pair (QK^T and PV)."""
+    total = 0
+    for b in reqs:
+        n = int(step.query_start_loc[b + 1] - step.query_start_loc[b])
+        c = int(step.context_lens[b])
+        pairs = n * c + n * (n + 1) // 2
+        total += 4 * step.head_dim * step.num_q_heads * pairs
+    return total
+
+
+def time_steps(fn, steps, stream):
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline
+# ---------------------------------------------------------------------------
+
+def oracle_sample(pool, step, fraction=8):
+    """1/fraction of the mixed step: every fraction-th request of each kind."""
+    from paged_kv_cache_284_gb300 import workloads
+    ql = step.q_lens.tolist()
+    kinds = {}
+    for b, n in enumerate(ql):
+        kinds.setdefault(n, []).append(b)
+    idx = []
+    for n, bs in sorted(kinds.items()):
+        idx += bs[::fraction]
+    return workloads.subset(step, sorted(idx))
+
+
+def time_oracle(pool, sub):
+    import oracle
+    t0 = time.perf_counter()
+    kb, vb = oracle.write_kv(sub.k, sub.v, sub.slot_mapping, pool.k_cache, pool.v_cache)
+    oracle.attention(sub.q, kb, vb, sub.block_tables, sub.query_start_loc, sub.context_lens,
+                     sub.seq_lens, sub.scale)
+    return time.perf_counter() - t0
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def traffic_for(kernel: str):
+    """dram bytes per KV byte from the committed ncu summary, if the kernel
+    source is unchanged since it was captured."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if sha != rec["source_sha256_16"]:
+        return None
+    return rec
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_cache_284_gb300 import workloads
+    oracle.build_oracle()
+    pool, (step,) = workloads.mixed_step()
+    sub = oracle_sample(pool, step)
+    for _ in range(args.warmup):
+        time_oracle(pool, sub)
+    t = 0.0
+    for _ in range(args.steps):
+        t += time_oracle(pool, sub)
+    tok = sub.num_q_tokens * args.steps
+    value = tok / t
+    cores = os.cpu_count()
+    sample = (f"1/8 of the mixed step per timed step ({sub.num_seqs} requests, "
+              f"{sub.num_q_tokens} query tokens): oracle write_kv + attention, fp64")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "query tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * t / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "query tokens/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "query tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_ours(args):
+    import paged_kv_cache_284_gb300 as pk
+    from paged_kv_cache_284_gb300 import workloads
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    hbm_peak, tc_peak, tc_peak_sus, peak_src = peaks()
+
+    # ---- headline: the mixed step ------------------------------------------
+    t0 = time.time()
+    pool, (step,) = workloads.mixed_step(seed=workloads.SEED_BASE + 3 + 1000 * rank)
+    log(f"[bench] mixed step generated in {time.time() - t0:.1f}s: "
+        f"{step.num_seqs} requests, {step.num_q_tokens} tokens, {pool.num_blocks} blocks")
+    ds = DeviceStep(pool, step, dev)
+    stream = torch.cuda.current_stream()
+    short_reqs = split_rows(step)
+    long_reqs = [b for b in range(step.num_seqs) if b not in set(short_reqs)]
+    short_bytes = algorithmic_bytes(step, short_reqs)
+    long_flops = tensor_core_flops(step, long_reqs)
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    # warm-up: at least W steps, and at least ~0.5 s of load so the clock
+    # samples cover a busy GPU
+    ds.run()
+    torch.cuda.synchronize()
+    t_w = time.time()
+    n_w = 0
+    while n_w < args.warmup or time.time() - t_w < 0.5:
+        ds.run()
+        n_w += 1
+        if n_w % 20 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+
+    # timed region: exactly K steps, kernel events for the two attention kernels
+    ev = {w: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)] for w in (pk.PA_KERNEL_SPLIT_KV,
+                                                     pk.PA_KERNEL_TENSOR_CORE)}
+    it = [0]
+
+    def timed_step():
+        i = it[0]
+        for w, pairs in ev.items():
+            pk.set_profile_events(w, *pairs[i])
+        ds.run()
+        it[0] += 1
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ms = time_steps(timed_step, args.steps, stream)
+    torch.cuda.synchronize()
+    for w in ev:
+        pk.set_profile_events(w, None, None)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = sampler.stop() if sampler else None
+    status = pk.read_device_status(clear=True)
+    if status:
+        log(f"[bench] WARNING device status {status:#x}")
+
+    ms_step = ms / args.steps
+    value = world * step.num_q_tokens * args.steps / (ms / 1000.0)
+    short_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[pk.PA_KERNEL_SPLIT_KV])
+    long_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[pk.PA_KERNEL_TENSOR_CORE])
+    achieved = short_bytes / (short_ms / 1000.0) / 1e9
+    tr = traffic_for("split_kv_mixed_step")
+    traffic = None
+    if tr:
+        traffic = tr["dram_bytes_per_algorithmic_byte"] * short_bytes
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": traffic,
+                "kernel": "split-KV decode/short-q kernel (pa_short.cu)",
+                "kernel_ms": short_ms, "algorithmic_bytes": short_bytes,
+                "peak_source": f"{peak_src} hbm_gbs (copy)"}
+    tflops = long_flops / (long_ms / 1000.0) / 1e12
+    tensor_core = {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
+                   "frac": tflops / tc_peak, "kernel": "tcgen05 prefill kernel (pa_long.cu)",
+                   "kernel_ms": long_ms, "flops": long_flops,
+                   "peak_source": f"{peak_src} bf16_tflops (burst)"}
+
+    # ---- e2e through the public API with host buffers ----------------------
+    e2e = None
+    if not args.no_e2e:
+        host = {name: t.cpu().pin_memory() for name, t in
+                (("q", step.q), ("k", step.k), ("v", step.v), ("slots", step.slot_mapping),
+                 ("bt", step.block_tables), ("qsl", step.query_start_loc),
+                 ("ctx", step.context_lens), ("sl", step.seq_lens))}
+        out_h = torch.empty(ds.out.shape, dtype=ds.out.dtype).pin_memory()
+        lse_h = torch.empty(ds.lse.shape, dtype=ds.lse.dtype).pin_memory()
+        dbuf = {name: torch.empty_like(t, device=dev) for name, t in host.items()}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+        def e2e_step():
+            for name, t in host.items():
+                dbuf[name].copy_(t, non_blocking=True)
+            pk.pa_write_kv(dbuf["k"], dbuf["v"], dbuf["slots"], ds.kc, ds.vc)
+            pk.pa_attention(dbuf["q"], ds.kc, ds.vc, dbuf["bt"], dbuf["qsl"], dbuf["ctx"],
+                            dbuf["sl"], step.scale, ds.out, ds.lse, workspace=ds.ws)
+            out_h.copy_(ds.out, non_blocking=True)
+            lse_h.copy_(ds.lse, non_blocking=True)
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e_ms = time_steps(e2e_step, args.steps, stream)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * step.num_q_tokens * args.steps / (e_ms / 1000.0),
+               "unit": "query tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms / args.steps}
+
+    gpu_launches = 4 * args.steps   # write_kv, plan, split-KV, tensor-core per step
+
+    # ---- secondary: decode-heavy KV GB/s and cascade --------------------------
+    decode = cascade = None
+    del ds
+    torch.cuda.empty_cache()
+    if not args.no_secondary:
+        decode = bench_decode_heavy(args, dev, hbm_peak)
+        cascade = bench_cascade(args, dev)
+
+    # ---- CPU baseline (rank 0 only) -----------------------------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        oracle.build_oracle()
+        sub = oracle_sample(pool, step)
+        t_cpu = time_oracle(pool, sub)
+        cpu = {"value": sub.num_q_tokens / t_cpu, "unit": "query tokens/s",
+               "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"1/8 of the mixed step ({sub.num_seqs} requests, "
+                         f"{sub.num_q_tokens} query tokens: every 8th chunk, decode and spec "
+                         f"request), fp64 oracle write_kv + attention, {t_cpu:.2f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "query tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "requests": step.num_seqs,
+                       "query_tokens": step.num_q_tokens, "pool_blocks": pool.num_blocks,
+                       "kv_bytes_read_per_step": kv_bytes(step, range(step.num_seqs)),
+                       "l2": "inputs larger than L2 (no flush needed)",
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "seed": workloads.SEED_BASE + 3},
+            "roofline": roofline,
+            "tensor_core": tensor_core,
+            "decode_heavy": decode,
+            "cascade": cascade,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clocks,
+            "gpu_launches": gpu_launches,
+            "device_status": status,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def bench_decode_heavy(args, dev, hbm_peak):
+    import paged_kv_cache_284_gb300 as pk
+    from paged_kv_cache_284_gb300 import workloads
+    pool, (step,) = workloads.decode_heavy()
+    ds = DeviceStep(pool, step, dev)
+    ds.run()
+    for _ in range(max(3, args.warmup)):
+        ds.run(write=False)
+    torch.cuda.synchronize()
+    s_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    it = [0]
+
+    def one():
+        pk.set_profile_events(pk.PA_KERNEL_SPLIT_KV, *s_ev[it[0]])
+        ds.run(write=False)
+        it[0] += 1
+
+    ms = time_steps(one, args.steps, torch.cuda.current_stream()) / args.steps
+    pk.set_profile_events(pk.PA_KERNEL_SPLIT_KV, None, None)
+    k_ms = statistics.mean(a.elapsed_time(b) for a, b in s_ev)
+    reqs = range(step.num_seqs)
+    kvb = kv_bytes(step, reqs)
+    alg = algorithmic_bytes(step, reqs)
+    res = {"workload": "256 decode rows, seq_len U[512,4096], 32 q / 8 kv heads, d=128, bs=16",
+           "kv_bytes": kvb, "attention_ms": ms, "kv_gbs": kvb / (ms / 1000) / 1e9,
+           "kv_frac_of_hbm": kvb / (ms / 1000) / 1e9 / hbm_peak,
+           "split_kv_kernel_ms": k_ms,
+           "split_kv_kernel_gbs": alg / (k_ms / 1000) / 1e9,
+           "split_kv_kernel_frac": alg / (k_ms / 1000) / 1e9 / hbm_peak}
+    del ds
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_cascade(args, dev):
+    import paged_kv_cache_284_gb300 as pk
+    from paged_kv_cache_284_gb300 import workloads
+    pool, (step,) = workloads.cascade()
+    ds = DeviceStep(pool, step, dev)
+    ds.run()
+    pb = step.prefix_blocks.to(dev)
+    sbt = step.suffix_block_tables.to(dev)
+    sctx = step.suffix_context_lens.to(dev)
+    ssl = step.suffix_seq_lens.to(dev)
+    out = torch.empty_like(ds.q)
+    lse = torch.empty_like(ds.lse)
+    ws = pk.alloc_workspace(pk.cascade_workspace_size(step.num_seqs, step.num_q_tokens,
+                                                      step.num_q_heads, step.num_kv_heads,
+                                                      step.head_dim, step.prefix_len), dev)
+
+    def casc():
+        pk.pa_cascade_decode(ds.q, ds.kc, ds.vc, pb, step.prefix_len, sbt, ds.qsl, sctx, ssl,
+                             step.scale, out, lse, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        casc()
+        ds.run(write=False)
+    torch.cuda.synchronize()
+    ms_c = time_steps(casc, args.steps, torch.cuda.current_stream()) / args.steps
+    ms_p = time_steps(lambda: ds.run(write=False), args.steps,
+                      torch.cuda.current_stream()) / args.steps
+    uniq = sum(int(s) for s in step.suffix_seq_lens) * step.num_kv_heads * step.head_dim * 4
+    pref = step.prefix_len * step.num_kv_heads * step.head_dim * 4
+    res = {"workload": "64 requests sharing an 8192-token prefix, suffix U[128,1024], q_len 1",
+           "cascade_ms": ms_c, "paged_attention_ms": ms_p, "speedup": ms_p / ms_c,
+           "cascade_algorithmic_kv_bytes": uniq + pref,
+           "cascade_kv_gbs": (uniq + pref) / (ms_c / 1000) / 1e9}
+    del ds
+    torch.cuda.empty_cache()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,675 @@
+// pa_api.cu -- the C ABI of libpa (declared in include/pa.h): argument checks,
+// TMA tensor maps, workspace layout and the launch sequence of one step.
+// Every step of the path runs in this library's kernels; nothing here
+// computes on the host beyond integer bookkeeping.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <algorithm>
+#include <mutex>
+#include <vector>
+
+#include "pa_internal.cuh"
+
+using namespace pa;
+
+// Per-device status word (PA_DEV_* bits).  Host code passes its device
+// address to the kernels; pa_read_device_status reads it back.
+__device__ unsigned int g_pa_status;
+
+namespace {
+
+thread_local char g_err[256] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int short_ctas_per_sm[2] = {0, 0};  // head_dim 64, 128
+    unsigned *status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_info(DeviceInfo **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return fail(PA_ERR_CUDA, "no current CUDA device");
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        void *sym = nullptr;
+        if (cudaGetSymbolAddress(&sym, g_pa_status) != cudaSuccess)
+            return fail(PA_ERR_CUDA, "cudaGetSymbolAddress(status) failed");
+        d.status = static_cast<unsigned *>(sym);
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return fail(PA_ERR_CUDA, "cannot query SM count");
+        d.short_ctas_per_sm[0] = short_max_ctas_per_sm(64);
+        d.short_ctas_per_sm[1] = short_max_ctas_per_sm(128);
+        d.ready = true;
+    }
+    *out = &d;
+    return PA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D view of one cache array: rows = (block, kv head, offset) flattened,
+// head_dim columns; boxes of 16 rows x 64 columns, 128-byte swizzle.
+int make_kv_map(CUtensorMap *m, void *base, int64_t rows, int head_dim) {
+    auto fn = encode_fn();
+    if (!fn) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kChunkKeys)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : fail(PA_ERR_CUDA, "KV tensor map encode failed (%d)", (int)r);
+}
+
+// 3-D view of q [tokens][q heads][head_dim]; a box is 64 dims x group heads x
+// tile tokens, i.e. the 128 (token, head) rows of one tensor-core tile.
+int make_q_map(CUtensorMap *m, const void *q, int tokens, int heads, int head_dim, int group,
+               int tile_tokens) {
+    auto fn = encode_fn();
+    if (!fn) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(heads),
+                          static_cast<cuuint64_t>(tokens > 0 ? tokens : 1)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                             static_cast<cuuint64_t>(heads) * head_dim * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(tile_tokens)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : fail(PA_ERR_CUDA, "Q tensor map encode failed (%d)", (int)r);
+}
+
+// Profiling hook state (pa_set_profile_events).
+void *g_prof[4][2] = {};
+std::mutex g_prof_mu;
+
+struct ProfScope {
+    int which;
+    cudaStream_t s;
+    void *end;
+    ProfScope(int w, cudaStream_t st) : which(w), s(st), end(nullptr) {
+        void *start;
+        {
+            std::lock_guard<std::mutex> lock(g_prof_mu);
+            start = g_prof[w][0];
+            end = g_prof[w][1];
+        }
+        if (start) cudaEventRecord(static_cast<cudaEvent_t>(start), s);
+    }
+    ~ProfScope() {
+        if (end) cudaEventRecord(static_cast<cudaEvent_t>(end), s);
+    }
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int q_tile_tokens(int group) { return group <= kLongRows ? kLongRows / group : 0; }
+
+WsLayout make_layout(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads,
+                     int head_dim, int prefix_partial_rows, bool with_extra) {
+    WsLayout L{};
+    const int group = num_q_heads / num_kv_heads;
+    const int tq = q_tile_tokens(group);
+    L.max_short = num_kv_heads * num_seqs * 8 + 4096;
+    L.max_long = num_kv_heads * ((num_q_tokens + tq - 1) / tq + num_seqs);
+    L.cap_rows = L.max_short * 8;
+    if (prefix_partial_rows > L.cap_rows) L.cap_rows = prefix_partial_rows;
+    L.num_counters = num_kv_heads * (num_seqs > 0 ? num_seqs : 1);
+    const int prefix_counters = num_kv_heads * ((num_q_tokens + tq - 1) / tq + 1);
+    if (with_extra && prefix_counters > L.num_counters) L.num_counters = prefix_counters;
+    size_t off = 0;
+    L.header = off;
+    off = align256(off + sizeof(PlanHeader));
+    L.counters = off;
+    off = align256(off + sizeof(int) * static_cast<size_t>(L.num_counters));
+    L.short_items = off;
+    off = align256(off + sizeof(ShortItem) * static_cast<size_t>(L.max_short));
+    L.long_items = off;
+    off = align256(off + sizeof(LongItem) * static_cast<size_t>(L.max_long));
+    L.partial_o = off;
+    off = align256(off + sizeof(float) * static_cast<size_t>(L.cap_rows) * head_dim);
+    L.partial_lse = off;
+    off = align256(off + sizeof(float) * static_cast<size_t>(L.cap_rows));
+    if (with_extra) {
+        const size_t rows = static_cast<size_t>(num_q_tokens) * num_q_heads;
+        L.extra_o = off;
+        off = align256(off + sizeof(float) * rows * head_dim);
+        L.extra_lse = off;
+        off = align256(off + sizeof(float) * rows);
+    }
+    L.total = off;
+    return L;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_kv(const pa_kv_desc *kv) {
+    if (!kv) return fail(PA_ERR_INVALID_ARG, "kv descriptor is NULL");
+    if (!kv->k_cache || !kv->v_cache) return fail(PA_ERR_INVALID_ARG, "cache pointer is NULL");
+    if (!aligned(kv->k_cache, 16) || !aligned(kv->v_cache, 16))
+        return fail(PA_ERR_INVALID_ARG, "cache pointers must be 16-byte aligned");
+    if (kv->num_blocks <= 0 || kv->num_kv_heads <= 0)
+        return fail(PA_ERR_INVALID_ARG, "num_blocks and num_kv_heads must be positive");
+    if (kv->head_dim != 64 && kv->head_dim != 128)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim %d not built (64 or 128)", kv->head_dim);
+    if (kv->block_size <= 0 || kv->block_size % 16 != 0 || kv->block_size > 256)
+        return fail(PA_ERR_UNSUPPORTED, "block_size %d: need a multiple of 16, at most 256",
+                    kv->block_size);
+    const int64_t rows = static_cast<int64_t>(kv->num_blocks) * kv->num_kv_heads * kv->block_size;
+    if (rows >= (static_cast<int64_t>(1) << 31) - 256)
+        return fail(PA_ERR_UNSUPPORTED, "pool too large: %lld cache rows", (long long)rows);
+    return PA_OK;
+}
+
+int check_heads(const pa_kv_desc *kv, int num_q_heads) {
+    if (num_q_heads <= 0 || num_q_heads % kv->num_kv_heads != 0)
+        return fail(PA_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d",
+                    num_q_heads, kv->num_kv_heads);
+    const int group = num_q_heads / kv->num_kv_heads;
+    if (group > kLongRows || group > 255)
+        return fail(PA_ERR_UNSUPPORTED, "group size %d too large", group);
+    return PA_OK;
+}
+
+int64_t kv_rows(const pa_kv_desc *kv) {
+    return static_cast<int64_t>(kv->num_blocks) * kv->num_kv_heads * kv->block_size;
+}
+
+struct StepMaps {
+    CUtensorMap q, k, v;
+};
+
+int make_maps(StepMaps *m, const void *q, const pa_kv_desc *kv, int tokens, int heads) {
+    const int group = heads / kv->num_kv_heads;
+    int rc = make_kv_map(&m->k, kv->k_cache, kv_rows(kv), kv->head_dim);
+    if (rc == PA_OK) rc = make_kv_map(&m->v, kv->v_cache, kv_rows(kv), kv->head_dim);
+    if (rc == PA_OK)
+        rc = make_q_map(&m->q, q, tokens, heads, kv->head_dim, group, q_tile_tokens(group));
+    return rc;
+}
+
+// Runs the planner, the split-KV kernel and the tensor-core kernel of one
+// step on `s`.  extra_o/extra_lse (cascade prefix state) may be NULL.
+int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, int32_t max_blocks,
+             const int32_t *qsl, const int32_t *ctx, const int32_t *seq_lens, int32_t num_seqs,
+             int32_t T, int32_t Hq, float scale, void *out, float *lse, uint8_t *ws,
+             const WsLayout &L, int short_max_rows, int split_keys, const float *extra_o,
+             const float *extra_lse, bool forbid_long, const StepMaps &maps, DeviceInfo *dev,
+             cudaStream_t s) {
+    const int D = kv->head_dim;
+    const int group = Hq / kv->num_kv_heads;
+    const int tq = q_tile_tokens(group);
+    PlanHeader *hdr = reinterpret_cast<PlanHeader *>(ws + L.header);
+
+    PlanParams pp{};
+    pp.qsl = qsl;
+    pp.ctx = ctx;
+    pp.seq_lens = seq_lens;
+    pp.num_seqs = num_seqs;
+    pp.num_q_tokens = T;
+    pp.num_kv_heads = kv->num_kv_heads;
+    pp.group = group;
+    pp.q_tile_tokens = tq;
+    pp.short_max_rows = forbid_long ? 0x7fffffff : short_max_rows;
+    pp.split_stages = split_keys / kStageKeys;
+    const int short_grid = dev->sms * dev->short_ctas_per_sm[D == 128 ? 1 : 0];
+    pp.target_items = 12 * short_grid;
+    pp.hdr = hdr;
+    pp.short_items = reinterpret_cast<ShortItem *>(ws + L.short_items);
+    pp.long_items = reinterpret_cast<LongItem *>(ws + L.long_items);
+    pp.counters = reinterpret_cast<int *>(ws + L.counters);
+    pp.max_short = L.max_short;
+    pp.max_long = L.max_long;
+    pp.cap_rows = L.cap_rows;
+    pp.num_counters = L.num_counters;
+    pp.status = dev->status;
+    int rc;
+    {
+        ProfScope prof(PA_KERNEL_PLAN, s);
+        rc = launch_plan(pp, s);
+    }
+    if (rc != PA_OK) return fail(rc, "plan launch failed");
+
+    ShortParams sp{};
+    sp.q = static_cast<const __nv_bfloat16 *>(q);
+    sp.out = static_cast<__nv_bfloat16 *>(out);
+    sp.lse = lse;
+    sp.block_tables = block_tables;
+    sp.bt_stride = max_blocks;
+    sp.qsl = qsl;
+    sp.ctx = ctx;
+    sp.seq_lens = seq_lens;
+    sp.num_q_heads = Hq;
+    sp.num_kv_heads = kv->num_kv_heads;
+    sp.group = group;
+    sp.block_size = kv->block_size;
+    sp.num_blocks = kv->num_blocks;
+    sp.kv_rows = static_cast<int>(kv_rows(kv));
+    sp.scale_log2 = scale * 1.4426950408889634f;
+    sp.hdr = hdr;
+    sp.items = pp.short_items;
+    sp.counters = pp.counters;
+    sp.partial_o = reinterpret_cast<float *>(ws + L.partial_o);
+    sp.partial_lse = reinterpret_cast<float *>(ws + L.partial_lse);
+    sp.extra_o = extra_o;
+    sp.extra_lse = extra_lse;
+    sp.status = dev->status;
+    {
+        ProfScope prof(PA_KERNEL_SPLIT_KV, s);
+        rc = launch_short(sp, maps.k, maps.v, D, short_grid, s);
+    }
+    if (rc != PA_OK) return fail(rc, "split-KV kernel launch failed: %s",
+                                 cudaGetErrorString(cudaGetLastError()));
+
+    if (!forbid_long) {
+        LongParams lp{};
+        lp.out = sp.out;
+        lp.lse = lse;
+        lp.out_f32 = nullptr;
+        lp.block_tables = block_tables;
+        lp.bt_stride = max_blocks;
+        lp.qsl = qsl;
+        lp.ctx = ctx;
+        lp.seq_lens = seq_lens;
+        lp.num_q_tokens = T;
+        lp.num_q_heads = Hq;
+        lp.num_kv_heads = kv->num_kv_heads;
+        lp.group = group;
+        lp.q_tile_tokens = tq;
+        lp.block_size = kv->block_size;
+        lp.num_blocks = kv->num_blocks;
+        lp.kv_rows = sp.kv_rows;
+        lp.scale_log2 = sp.scale_log2;
+        lp.prefix_mode = 0;
+        lp.hdr = hdr;
+        lp.items = pp.long_items;
+        lp.counters = pp.counters;
+        lp.partial_o = sp.partial_o;
+        lp.partial_lse = sp.partial_lse;
+        lp.status = dev->status;
+        // a long request has q_len * group > short_max_rows, so there are at
+        // most T / (short_max_rows / group + 1) of them
+        const int min_long_tokens = short_max_rows / group + 1;
+        const int max_long_reqs = std::min(num_seqs, T / std::max(1, min_long_tokens));
+        const int grid = kv->num_kv_heads * ((T + tq - 1) / tq + max_long_reqs);
+        {
+            ProfScope prof(PA_KERNEL_TENSOR_CORE, s);
+            rc = launch_long(lp, maps.q, maps.k, maps.v, D, std::min(grid, L.max_long), s);
+        }
+        if (rc != PA_OK) return fail(rc, "tensor-core kernel launch failed: %s",
+                                     cudaGetErrorString(cudaGetLastError()));
+    }
+    return PA_OK;
+}
+
+int common_checks(const void *q, const pa_kv_desc *kv, int32_t num_q_tokens, int32_t num_q_heads,
+                  float scale, const void *out, const void *workspace) {
+    int rc = check_kv(kv);
+    if (rc != PA_OK) return rc;
+    rc = check_heads(kv, num_q_heads);
+    if (rc != PA_OK) return rc;
+    if (num_q_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_q_tokens < 0");
+    if (num_q_tokens > 0 && (!q || !out)) return fail(PA_ERR_INVALID_ARG, "q or out is NULL");
+    if (!aligned(q, 16) || !aligned(out, 16))
+        return fail(PA_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+    if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale is not finite");
+    if (workspace && !aligned(workspace, 256))
+        return fail(PA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    return PA_OK;
+}
+
+int prefix_plan(int T, int prefix_len, int num_kv_heads, int group, int sms, int *q_tiles,
+                int *nsplit, int *split_keys) {
+    const int tq = q_tile_tokens(group);
+    *q_tiles = (T + tq - 1) / tq;
+    const int tiles = (prefix_len + kLongKeys - 1) / kLongKeys;
+    const int pairs = num_kv_heads * *q_tiles;
+    int ns = (2 * sms + pairs - 1) / pairs;
+    ns = std::max(1, std::min(ns, std::min(64, tiles)));
+    const int per = (tiles + ns - 1) / ns;  // KV tiles per split
+    *split_keys = per * kLongKeys;
+    *nsplit = (prefix_len + *split_keys - 1) / *split_keys;
+    if (*nsplit < 1) *nsplit = 1;
+    return PA_OK;
+}
+
+int run_prefix(const void *q, const pa_kv_desc *kv, const int32_t *prefix_blocks, int32_t prefix_len,
+               int32_t T, int32_t Hq, float scale, void *out, float *out_f32, float *lse,
+               uint8_t *ws, const WsLayout &L, const StepMaps &maps, DeviceInfo *dev,
+               cudaStream_t s) {
+    const int group = Hq / kv->num_kv_heads;
+    int q_tiles, nsplit, split_keys;
+    prefix_plan(T, prefix_len, kv->num_kv_heads, group, dev->sms, &q_tiles, &nsplit, &split_keys);
+    int *counters = reinterpret_cast<int *>(ws + L.counters);
+    if (nsplit > 1 &&
+        cudaMemsetAsync(counters, 0, sizeof(int) * kv->num_kv_heads * q_tiles, s) != cudaSuccess)
+        return fail(PA_ERR_CUDA, "counter reset failed");
+    LongParams lp{};
+    lp.out = static_cast<__nv_bfloat16 *>(out);
+    lp.lse = lse;
+    lp.out_f32 = out_f32;
+    lp.block_tables = prefix_blocks;
+    lp.bt_stride = 0;
+    lp.num_q_tokens = T;
+    lp.num_q_heads = Hq;
+    lp.num_kv_heads = kv->num_kv_heads;
+    lp.group = group;
+    lp.q_tile_tokens = q_tile_tokens(group);
+    lp.block_size = kv->block_size;
+    lp.num_blocks = kv->num_blocks;
+    lp.kv_rows = static_cast<int>(kv_rows(kv));
+    lp.scale_log2 = scale * 1.4426950408889634f;
+    lp.prefix_mode = 1;
+    lp.prefix_len = prefix_len;
+    lp.prefix_nsplit = nsplit;
+    lp.prefix_split_keys = split_keys;
+    lp.prefix_q_tiles = q_tiles;
+    lp.counters = counters;
+    lp.partial_o = reinterpret_cast<float *>(ws + L.partial_o);
+    lp.partial_lse = reinterpret_cast<float *>(ws + L.partial_lse);
+    lp.status = dev->status;
+    const int grid = kv->num_kv_heads * q_tiles * nsplit;
+    const int rc = launch_long(lp, maps.q, maps.k, maps.v, kv->head_dim, grid, s);
+    if (rc != PA_OK) return fail(rc, "prefix kernel launch failed");
+    return PA_OK;
+}
+
+int prefix_partial_rows(int T, int prefix_len, int num_kv_heads, int group) {
+    int q_tiles, nsplit, split_keys;
+    // the split count never exceeds 64, whatever the SM count
+    prefix_plan(T, prefix_len, num_kv_heads, group, 1 << 20, &q_tiles, &nsplit, &split_keys);
+    return num_kv_heads * q_tiles * nsplit * kLongRows;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_last_error_message(void) { return g_err; }
+
+const char *pa_status_string(int code) {
+    switch (code) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_BAD_METADATA: return "PA_ERR_BAD_METADATA";
+    default: return "PA_ERR_UNKNOWN";
+    }
+}
+
+int pa_write_kv(const void *k, const void *v, const int64_t *slot_mapping, int32_t num_tokens,
+                const pa_kv_desc *kv, void *stream) {
+    g_err[0] = 0;
+    int rc = check_kv(kv);
+    if (rc != PA_OK) return rc;
+    if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !slot_mapping) return fail(PA_ERR_INVALID_ARG, "NULL input");
+    if (!aligned(k, 16) || !aligned(v, 16))
+        return fail(PA_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+    DeviceInfo *dev;
+    if ((rc = device_info(&dev)) != PA_OK) return rc;
+    {
+        ProfScope prof(PA_KERNEL_WRITE_KV, static_cast<cudaStream_t>(stream));
+        rc = launch_write_kv(k, v, slot_mapping, num_tokens, kv, dev->status,
+                             static_cast<cudaStream_t>(stream));
+    }
+    return rc == PA_OK ? PA_OK : fail(rc, "write_kv launch failed");
+}
+
+size_t pa_attention_workspace_size(int32_t num_seqs, int32_t num_q_tokens, int32_t num_q_heads,
+                                   int32_t num_kv_heads, int32_t head_dim) {
+    if (num_seqs < 0 || num_q_tokens < 0 || num_kv_heads <= 0 || num_q_heads <= 0 ||
+        num_q_heads % num_kv_heads != 0 || (head_dim != 64 && head_dim != 128))
+        return 0;
+    return make_layout(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, 0, false).total;
+}
+
+int pa_attention_ex(const void *q, const pa_kv_desc *kv, const int32_t *block_tables,
+                    int32_t max_blocks_per_seq, const int32_t *query_start_loc,
+                    const int32_t *context_lens, const int32_t *seq_lens, int32_t num_seqs,
+                    int32_t num_q_tokens, int32_t num_q_heads, float scale, void *out, float *lse,
+                    void *workspace, size_t workspace_bytes, int32_t short_q_max_rows,
+                    int32_t split_keys, void *stream) {
+    g_err[0] = 0;
+    int rc = common_checks(q, kv, num_q_tokens, num_q_heads, scale, out, workspace);
+    if (rc != PA_OK) return rc;
+    if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs < 0");
+    if (short_q_max_rows < -1 || short_q_max_rows > kShortMaxRows)
+        return fail(PA_ERR_INVALID_ARG, "short_q_max_rows must be -1 or in [0, %d]", kShortMaxRows);
+    if (split_keys < 0 || split_keys % kStageKeys != 0)
+        return fail(PA_ERR_INVALID_ARG, "split_keys must be 0 or a multiple of %d", kStageKeys);
+    if (num_seqs == 0 || num_q_tokens == 0) return PA_OK;
+    if (!block_tables || !query_start_loc || !context_lens || !seq_lens)
+        return fail(PA_ERR_INVALID_ARG, "metadata pointer is NULL");
+    if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq <= 0");
+    const WsLayout L = make_layout(num_seqs, num_q_tokens, num_q_heads, kv->num_kv_heads,
+                                   kv->head_dim, 0, false);
+    if (!workspace || workspace_bytes < L.total)
+        return fail(PA_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", L.total,
+                    workspace_bytes);
+    DeviceInfo *dev;
+    if ((rc = device_info(&dev)) != PA_OK) return rc;
+    StepMaps maps;
+    if ((rc = make_maps(&maps, q, kv, num_q_tokens, num_q_heads)) != PA_OK) return rc;
+    return run_step(q, kv, block_tables, max_blocks_per_seq, query_start_loc, context_lens,
+                    seq_lens, num_seqs, num_q_tokens, num_q_heads, scale, out, lse,
+                    static_cast<uint8_t *>(workspace), L,
+                    short_q_max_rows < 0 ? kShortMaxRows : short_q_max_rows, split_keys, nullptr,
+                    nullptr, false, maps, dev, static_cast<cudaStream_t>(stream));
+}
+
+int pa_attention(const void *q, const pa_kv_desc *kv, const int32_t *block_tables,
+                 int32_t max_blocks_per_seq, const int32_t *query_start_loc,
+                 const int32_t *context_lens, const int32_t *seq_lens, int32_t num_seqs,
+                 int32_t num_q_tokens, int32_t num_q_heads, float scale, void *out, float *lse,
+                 void *workspace, size_t workspace_bytes, void *stream) {
+    return pa_attention_ex(q, kv, block_tables, max_blocks_per_seq, query_start_loc, context_lens,
+                           seq_lens, num_seqs, num_q_tokens, num_q_heads, scale, out, lse,
+                           workspace, workspace_bytes, -1, 0, stream);
+}
+
+int pa_merge_states(const void *o_a, const float *lse_a, const void *o_b, const float *lse_b,
+                    int32_t n, int32_t num_heads, int32_t head_dim, void *out, float *lse_out,
+                    void *stream) {
+    g_err[0] = 0;
+    if (n < 0 || num_heads <= 0) return fail(PA_ERR_INVALID_ARG, "bad n / num_heads");
+    if (head_dim <= 0 || head_dim % 8 != 0)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim must be a positive multiple of 8");
+    if (n == 0) return PA_OK;
+    if (!o_a || !o_b || !lse_a || !lse_b || !out) return fail(PA_ERR_INVALID_ARG, "NULL input");
+    if (!aligned(o_a, 16) || !aligned(o_b, 16) || !aligned(out, 16))
+        return fail(PA_ERR_INVALID_ARG, "o_a, o_b and out must be 16-byte aligned");
+    const int rc = launch_merge(o_a, lse_a, o_b, lse_b, n, num_heads, head_dim, out, lse_out,
+                                static_cast<cudaStream_t>(stream));
+    return rc == PA_OK ? PA_OK : fail(rc, "merge launch failed");
+}
+
+size_t pa_cascade_workspace_size(int32_t num_seqs, int32_t num_q_tokens, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t prefix_len) {
+    if (num_seqs < 0 || num_q_tokens < 0 || num_kv_heads <= 0 || num_q_heads <= 0 ||
+        num_q_heads % num_kv_heads != 0 || (head_dim != 64 && head_dim != 128) || prefix_len < 0)
+        return 0;
+    const int group = num_q_heads / num_kv_heads;
+    const int rows = prefix_partial_rows(num_q_tokens, prefix_len, num_kv_heads, group);
+    return make_layout(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, rows, true)
+        .total;
+}
+
+int pa_prefix_attention(const void *q, const pa_kv_desc *kv, const int32_t *prefix_blocks,
+                        int32_t prefix_len, int32_t num_q_tokens, int32_t num_q_heads,
+                        float scale, void *out, float *lse, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+    g_err[0] = 0;
+    int rc = common_checks(q, kv, num_q_tokens, num_q_heads, scale, out, workspace);
+    if (rc != PA_OK) return rc;
+    if (prefix_len < 0) return fail(PA_ERR_INVALID_ARG, "prefix_len < 0");
+    if (prefix_len > 0 && !prefix_blocks) return fail(PA_ERR_INVALID_ARG, "prefix_blocks is NULL");
+    if (num_q_tokens == 0) return PA_OK;
+    const int group = num_q_heads / kv->num_kv_heads;
+    const WsLayout L = make_layout(1, num_q_tokens, num_q_heads, kv->num_kv_heads, kv->head_dim,
+                                   prefix_partial_rows(num_q_tokens, prefix_len, kv->num_kv_heads,
+                                                       group),
+                                   true);
+    if (!workspace || workspace_bytes < L.total)
+        return fail(PA_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", L.total,
+                    workspace_bytes);
+    DeviceInfo *dev;
+    if ((rc = device_info(&dev)) != PA_OK) return rc;
+    StepMaps maps;
+    if ((rc = make_maps(&maps, q, kv, num_q_tokens, num_q_heads)) != PA_OK) return rc;
+    return run_prefix(q, kv, prefix_blocks, prefix_len, num_q_tokens, num_q_heads, scale, out,
+                      nullptr, lse, static_cast<uint8_t *>(workspace), L, maps, dev,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int pa_cascade_decode(const void *q, const pa_kv_desc *kv, const int32_t *prefix_blocks,
+                      int32_t prefix_len, const int32_t *block_tables,
+                      int32_t max_blocks_per_seq, const int32_t *query_start_loc,
+                      const int32_t *context_lens, const int32_t *seq_lens, int32_t num_seqs,
+                      int32_t num_q_tokens, int32_t num_q_heads, float scale, void *out,
+                      float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+    g_err[0] = 0;
+    int rc = common_checks(q, kv, num_q_tokens, num_q_heads, scale, out, workspace);
+    if (rc != PA_OK) return rc;
+    if (num_seqs < 0 || prefix_len < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
+    if (prefix_len > 0 && !prefix_blocks) return fail(PA_ERR_INVALID_ARG, "prefix_blocks is NULL");
+    if (num_seqs == 0 || num_q_tokens == 0) return PA_OK;
+    if (!block_tables || !query_start_loc || !context_lens || !seq_lens)
+        return fail(PA_ERR_INVALID_ARG, "metadata pointer is NULL");
+    if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq <= 0");
+    const int group = num_q_heads / kv->num_kv_heads;
+    const WsLayout L = make_layout(num_seqs, num_q_tokens, num_q_heads, kv->num_kv_heads,
+                                   kv->head_dim,
+                                   prefix_partial_rows(num_q_tokens, prefix_len, kv->num_kv_heads,
+                                                       group),
+                                   true);
+    if (!workspace || workspace_bytes < L.total)
+        return fail(PA_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", L.total,
+                    workspace_bytes);
+    DeviceInfo *dev;
+    if ((rc = device_info(&dev)) != PA_OK) return rc;
+    StepMaps maps;
+    if ((rc = make_maps(&maps, q, kv, num_q_tokens, num_q_heads)) != PA_OK) return rc;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *xo = reinterpret_cast<float *>(ws + L.extra_o);
+    float *xl = reinterpret_cast<float *>(ws + L.extra_lse);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = run_prefix(q, kv, prefix_blocks, prefix_len, num_q_tokens, num_q_heads, scale, nullptr, xo,
+                    xl, ws, L, maps, dev, s);
+    if (rc != PA_OK) return rc;
+    return run_step(q, kv, block_tables, max_blocks_per_seq, query_start_loc, context_lens,
+                    seq_lens, num_seqs, num_q_tokens, num_q_heads, scale, out, lse, ws, L,
+                    kShortMaxRows, 0, xo, xl, true, maps, dev, s);
+}
+
+int pa_validate_metadata(const int32_t *block_tables, int32_t max_blocks_per_seq,
+                         const int32_t *query_start_loc, const int32_t *context_lens,
+                         const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_tokens,
+                         const int64_t *slot_mapping, int32_t num_blocks, int32_t block_size) {
+    g_err[0] = 0;
+    if (num_seqs < 0 || num_q_tokens < 0 || block_size <= 0 || num_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARG, "bad sizes");
+    if (num_seqs > 0 && (!block_tables || !query_start_loc || !context_lens || !seq_lens))
+        return fail(PA_ERR_INVALID_ARG, "metadata pointer is NULL");
+    if (num_seqs > 0 && query_start_loc[0] != 0)
+        return fail(PA_ERR_BAD_METADATA, "query_start_loc[0] = %d, expected 0", query_start_loc[0]);
+    for (int b = 0; b < num_seqs; ++b) {
+        const int n = query_start_loc[b + 1] - query_start_loc[b];
+        if (n < 0) return fail(PA_ERR_BAD_METADATA, "query_start_loc decreases at %d", b);
+        if (context_lens[b] < 0) return fail(PA_ERR_BAD_METADATA, "context_lens[%d] < 0", b);
+        if (seq_lens[b] != context_lens[b] + n)
+            return fail(PA_ERR_BAD_METADATA, "seq_lens[%d]=%d != context %d + q_len %d", b,
+                        seq_lens[b], context_lens[b], n);
+        const int64_t nblk = (static_cast<int64_t>(seq_lens[b]) + block_size - 1) / block_size;
+        if (nblk > max_blocks_per_seq)
+            return fail(PA_ERR_BAD_METADATA, "request %d needs %lld blocks > max_blocks_per_seq",
+                        b, (long long)nblk);
+        for (int64_t j = 0; j < nblk; ++j) {
+            const int32_t blk = block_tables[static_cast<int64_t>(b) * max_blocks_per_seq + j];
+            if (blk < 0 || blk >= num_blocks)
+                return fail(PA_ERR_BAD_METADATA, "block_tables[%d][%lld] = %d out of range", b,
+                            (long long)j, blk);
+        }
+    }
+    if (num_seqs > 0 && query_start_loc[num_seqs] != num_q_tokens)
+        return fail(PA_ERR_BAD_METADATA, "query_start_loc[num_seqs] = %d != num_q_tokens %d",
+                    query_start_loc[num_seqs], num_q_tokens);
+    if (slot_mapping && num_q_tokens > 0) {
+        const int64_t nslots = static_cast<int64_t>(num_blocks) * block_size;
+        // duplicates: mark slots in a bitmap
+        std::vector<uint8_t> seen(static_cast<size_t>((nslots + 7) / 8), 0);
+        for (int t = 0; t < num_q_tokens; ++t) {
+            const int64_t s = slot_mapping[t];
+            if (s < 0) continue;
+            if (s >= nslots) return fail(PA_ERR_BAD_METADATA, "slot_mapping[%d] = %lld outside pool", t, (long long)s);
+            uint8_t &byte = seen[static_cast<size_t>(s >> 3)];
+            const uint8_t bit = static_cast<uint8_t>(1u << (s & 7));
+            if (byte & bit) return fail(PA_ERR_BAD_METADATA, "slot %lld used twice", (long long)s);
+            byte |= bit;
+        }
+    }
+    return PA_OK;
+}
+
+int pa_set_profile_events(int32_t which, void *start_event, void *end_event) {
+    g_err[0] = 0;
+    if (which < 0 || which > 3) return fail(PA_ERR_INVALID_ARG, "unknown kernel id %d", which);
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_prof[which][0] = start_event;
+    g_prof[which][1] = end_event;
+    return PA_OK;
+}
+
+int pa_read_device_status(uint32_t *status, int clear, void *stream) {
+    g_err[0] = 0;
+    if (!status) return fail(PA_ERR_INVALID_ARG, "status is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return fail(PA_ERR_CUDA, "stream sync failed");
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_pa_status, sizeof v) != cudaSuccess)
+        return fail(PA_ERR_CUDA, "status read failed");
+    *status = v;
+    if (clear) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_pa_status, &zero, sizeof zero) != cudaSuccess)
+            return fail(PA_ERR_CUDA, "status clear failed");
+    }
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,372 @@
+// pa_internal.cuh -- shared device helpers and plan structures of libpa.
+//
+// Inline-PTX wrappers for the sm_100-family async machinery the kernels use:
+// mbarriers with bounded waits, TMA tensor loads (cp.async.bulk.tensor),
+// tcgen05 MMA / TMEM, and the warp-level mma.sync used by the memory-bound
+// split-KV kernel.  Nothing here computes attention; the kernels do.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+// ---------------------------------------------------------------------------
+// Geometry shared by host planner and kernels
+// ---------------------------------------------------------------------------
+constexpr int kChunkKeys = 16;        // keys per TMA box (rows of one cache box)
+constexpr int kStageChunks = 4;       // split-KV kernel: chunks per pipeline stage
+constexpr int kStageKeys = kChunkKeys * kStageChunks;  // 64 keys per stage
+constexpr int kShortStages = 3;       // split-KV kernel: pipeline depth
+constexpr int kShortMaxRows = 64;     // rows (q_len * group) a split-KV item may hold
+constexpr int kShortConsumerWarps = 4;
+constexpr int kShortThreads = 32 * (kShortConsumerWarps + 1);
+constexpr int kLongRows = 128;        // tcgen05 tile: M = 128 query rows
+constexpr int kLongKeys = 128;        // tcgen05 tile: N = 128 keys per KV tile
+constexpr int kLongThreads = 192;     // 6 warps: TMA, MMA, 4 x softmax
+constexpr int kPlanThreads = 1024;
+constexpr int kMinSplitStages = 4;    // 256 keys: smallest automatic split
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
+
+// Work list written by the plan kernel into the caller's workspace.
+struct PlanHeader {
+    int num_short_items;
+    int num_long_items;
+    int short_next;        // dynamic work counter of the split-KV kernel
+    int long_next;         // dynamic work counter of the tensor-core kernel
+    int split_stages;      // chosen split size (in 64-key stages)
+    int partial_rows;      // partial-state rows used
+    int pad[10];
+};
+static_assert(sizeof(PlanHeader) == 64, "header size");
+
+// One split-KV work item: kv head h of request b, keys
+// [stage_begin*64, min(stage_end*64, seq_len)).
+struct ShortItem {
+    int b, h, split, nsplit;
+    int stage_begin, stage_end;
+    int partial_base;  // first partial row of this split (nsplit > 1)
+    int pad;
+};
+static_assert(sizeof(ShortItem) == 32, "item size");
+
+// One tensor-core work item: kv head h of request b, query tile q_tile
+// (tile = 128/group tokens x group heads), keys [key_begin, key_end).
+struct LongItem {
+    int b, h, q_tile, split, nsplit;
+    int key_begin, key_end;
+    int partial_base;
+};
+static_assert(sizeof(LongItem) == 32, "item size");
+
+// Byte offsets of the workspace regions (same computation on host and device).
+struct WsLayout {
+    size_t header, counters, short_items, long_items, partial_o, partial_lse, extra_o, extra_lse;
+    size_t total;
+    int max_short, max_long, cap_rows, num_counters;
+};
+
+// Kernel parameter blocks -----------------------------------------------------
+struct ShortParams {
+    const __nv_bfloat16 *q;
+    __nv_bfloat16 *out;
+    float *lse;
+    const int *block_tables;
+    int bt_stride;
+    const int *qsl, *ctx, *seq_lens;
+    int num_q_heads, num_kv_heads, group, block_size, num_blocks, kv_rows;
+    float scale_log2;
+    PlanHeader *hdr;
+    const ShortItem *items;
+    int *counters;
+    float *partial_o, *partial_lse;
+    const float *extra_o, *extra_lse;  // cascade: prefix state folded into the output
+    unsigned *status;
+};
+
+struct LongParams {
+    __nv_bfloat16 *out;
+    float *lse;
+    float *out_f32;          // if set, final output is written as fp32 state here
+    const int *block_tables;  // per-request tables, or the prefix block list
+    int bt_stride;            // 0 in prefix mode
+    const int *qsl, *ctx, *seq_lens;
+    int num_q_tokens, num_q_heads, num_kv_heads, group, q_tile_tokens, block_size, num_blocks,
+        kv_rows;
+    float scale_log2;
+    int prefix_mode;  // 1: non-causal shared prefix, items implicit
+    int prefix_len, prefix_nsplit, prefix_split_keys, prefix_q_tiles;
+    PlanHeader *hdr;
+    const LongItem *items;
+    int *counters;
+    float *partial_o, *partial_lse;
+    unsigned *status;
+};
+
+struct PlanParams {
+    const int *qsl, *ctx, *seq_lens;
+    int num_seqs, num_q_tokens, num_kv_heads, group, q_tile_tokens;
+    int short_max_rows;  // q_len*group <= this -> split-KV kernel
+    int split_stages;    // 0 = automatic
+    int target_items;    // automatic split aims at about this many split-KV items
+    PlanHeader *hdr;
+    ShortItem *short_items;
+    LongItem *long_items;
+    int *counters;
+    int max_short, max_long, cap_rows, num_counters;
+    unsigned *status;
+};
+
+// Host-side launchers (each defined next to its kernel).
+int launch_write_kv(const void *k, const void *v, const int64_t *slots, int num_tokens,
+                    const pa_kv_desc *kv, unsigned *status, cudaStream_t s);
+int launch_plan(const PlanParams &p, cudaStream_t s);
+int launch_short(const ShortParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                 int head_dim, int grid, cudaStream_t s);
+int short_max_ctas_per_sm(int head_dim);
+int launch_long(const LongParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                const CUtensorMap &tv, int head_dim, int grid, cudaStream_t s);
+int launch_merge(const void *oa, const float *la, const void *ob, const float *lb, int n,
+                 int heads, int head_dim, void *out, float *lse_out, cudaStream_t s);
+size_t short_smem_bytes(int head_dim);
+size_t long_smem_bytes(int head_dim);
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void flag_status(unsigned *status, unsigned bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// mbarrier ------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: gives up (returning false and raising *abort) when the
+// barrier phase has not completed within kWaitTimeoutNs, or as soon as
+// another thread of the CTA has raised *abort.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+// Short bounded wait used only while draining after an abort.
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > 100000000ull) break;
+    }
+}
+
+// TMA --------------------------------------------------------------------------
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *tm) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, int c0, int c1,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *tm, int c0, int c1,
+                                            int c2, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+// Order this thread's generic-proxy shared-memory accesses before later
+// async-proxy (TMA / tensor core) accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Named barrier among `count` threads (id 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Offset of 16-byte column `chunk` (0..7) of row `row` inside a tile written
+// by TMA with 128-byte swizzling (rows of 128 bytes, 1024-byte aligned base):
+// the hardware XORs the chunk index with the row index modulo 8.
+__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
+    return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// Warp-level tensor core (memory-bound split-KV kernel) ---------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                          uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// tcgen05 / TMEM -------------------------------------------------------------
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Shared-memory matrix descriptor (tcgen05): start address, leading- and
+// stride-dimension byte offsets (all >> 4), descriptor version 1 at bit 46,
+// swizzle mode in bits 61-63 (2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;
+    d |= 2ull << 61;
+    return d;
+}
+// Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulate.
+// b_mn_major: B operand stored N-contiguous (e.g. V rows for P*V).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_major) {
+    return (1u << 4)                                  // D format: f32
+           | (1u << 7)                                // A format: bf16
+           | (1u << 10)                               // B format: bf16
+           | (static_cast<uint32_t>(b_mn_major) << 16)  // B major-ness
+           | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// 32 lanes x 32 columns of 32-bit TMEM cells: thread i gets lane (base+i),
+// columns col..col+31.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// Attention-state folding -------------------------------------------------------
+// A state is (o normalised, lse natural log).  Fold partial states of one
+// (row, element): returns the merged o element and, via *lse_out, the merged
+// lse.  Empty states carry lse = -inf and contribute nothing.
+__device__ __forceinline__ float lse_max_of(const float *lse, int stride, int n, float extra) {
+    float m = extra;
+    for (int s = 0; s < n; ++s) m = fmaxf(m, __ldcg(lse + static_cast<size_t>(s) * stride));
+    return m;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace pa

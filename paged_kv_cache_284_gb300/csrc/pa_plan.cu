@@ -1,0 +1,229 @@
+// pa_plan.cu -- device-side step planner.
+//
+// From the step's AttentionMeta-style metadata (query_start_loc,
+// context_lens, seq_lens; "vLLM中如何实现大模型推理加速技术？": every attention
+// op carries each request's progress) it classifies each request, picks a
+// split-KV size and writes the two work lists into the workspace:
+//   * short rows (q_len * group <= short_max_rows: decode, speculative
+//     verify, small chunks) -> split-KV items (request, kv head, key range);
+//   * long rows (chunked-prefill chunks, prefix-hit prompts, whole prompts)
+//     -> tensor-core items (request, kv head, 128-row query tile).
+// Runs as one CTA so the whole step stays on the device (no host round trip,
+// capturable in a CUDA graph).  It also zeroes the split completion
+// counters and the dynamic work counters.
+#include "pa_internal.cuh"
+
+namespace pa {
+
+// Exclusive block-wide prefix sum over kPlanThreads threads.
+__device__ int block_exclusive_scan(int v, int *tmp, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) tmp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = (lane < (kPlanThreads / 32)) ? tmp[lane] : 0;
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += n;
+        }
+        tmp[lane] = wi - w;  // exclusive prefix of warp totals
+        if (lane == 31) tmp[32] = wi;
+    }
+    __syncthreads();
+    const int res = tmp[warp] + incl - v;
+    *total = tmp[32];
+    __syncthreads();
+    return res;
+}
+
+__device__ long long block_sum_ll(long long v, long long *tmp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) tmp[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        long long w = (lane < (kPlanThreads / 32)) ? tmp[lane] : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+        if (lane == 0) tmp[32] = w;
+    }
+    __syncthreads();
+    const long long r = tmp[32];
+    __syncthreads();
+    return r;
+}
+
+struct ReqInfo {
+    int n, ctx, len;
+    int is_short;
+    int stages;   // 64-key stages of a short request
+    int qtiles;   // query tiles of a long request
+};
+
+__device__ __forceinline__ ReqInfo load_req(const PlanParams &p, int b) {
+    ReqInfo r{};
+    const int q0 = p.qsl[b], q1 = p.qsl[b + 1];
+    r.n = q1 - q0;
+    r.ctx = p.ctx[b];
+    r.len = p.seq_lens[b];
+    const bool bad = r.n < 0 || r.ctx < 0 || r.len != r.ctx + r.n || q0 < 0 ||
+                     q1 > p.num_q_tokens;
+    if (bad) {
+        flag_status(p.status, PA_DEV_BAD_METADATA);
+        r.n = 0;
+    }
+    if (r.n > 0) {
+        r.is_short = (r.n * p.group <= p.short_max_rows) ? 1 : 0;
+        if (r.is_short)
+            r.stages = (r.len + kStageKeys - 1) / kStageKeys;
+        else
+            r.qtiles = (r.n + p.q_tile_tokens - 1) / p.q_tile_tokens;
+    }
+    return r;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
+    __shared__ int tmp[33];
+    __shared__ long long tmpl[33];
+    __shared__ int s_split;
+    __shared__ int s_overflow;
+    const int tid = threadIdx.x;
+    if (tid == 0) s_overflow = 0;
+    const int hkv = p.num_kv_heads;
+
+    // 1. total split-KV work (in stages) -------------------------------------
+    long long work = 0, max_stages = 0;
+    for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+        const ReqInfo r = load_req(p, b);
+        if (r.is_short) {
+            work += r.stages;
+            max_stages = max(max_stages, static_cast<long long>(r.stages));
+        }
+    }
+    const long long total_work = block_sum_ll(work, tmpl) * hkv;
+    // block max via the same reduction on negated values is awkward; use a
+    // shared atomic instead.
+    __shared__ int s_max_stages;
+    if (tid == 0) s_max_stages = 0;
+    __syncthreads();
+    atomicMax(&s_max_stages, static_cast<int>(max_stages));
+    __syncthreads();
+
+    // 2. split size ------------------------------------------------------------
+    int sp;
+    if (p.split_stages > 0) {
+        sp = p.split_stages;
+    } else {
+        const long long tgt = max(1, p.target_items);
+        sp = static_cast<int>(max(static_cast<long long>(kMinSplitStages),
+                                  (total_work + tgt - 1) / tgt));
+    }
+    for (int guard = 0; guard < 40; ++guard) {
+        long long items = 0, rows = 0;
+        for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+            const ReqInfo r = load_req(p, b);
+            if (!r.is_short) continue;
+            const int ns = (r.stages + sp - 1) / sp;
+            items += ns;
+            if (ns > 1) rows += static_cast<long long>(ns) * r.n * p.group;
+        }
+        items = block_sum_ll(items, tmpl) * hkv;
+        rows = block_sum_ll(rows, tmpl) * hkv;
+        if ((items <= p.max_short && rows <= p.cap_rows) || sp >= s_max_stages) break;
+        sp *= 2;
+    }
+    if (tid == 0) s_split = sp;
+    __syncthreads();
+    sp = s_split;
+
+    // 3. emit items, request by request in rounds of kPlanThreads -------------
+    int short_base = 0, long_base = 0, row_base = 0;
+    for (int b0 = 0; b0 < p.num_seqs; b0 += kPlanThreads) {
+        const int b = b0 + tid;
+        ReqInfo r{};
+        if (b < p.num_seqs) r = load_req(p, b);
+        const int ns = r.is_short ? (r.stages + sp - 1) / sp : 0;
+        const int R = r.n * p.group;
+        const int n_short = ns * hkv;
+        const int n_rows = (ns > 1) ? ns * R * hkv : 0;
+        const int n_long = r.qtiles * hkv;
+        int tot_s, tot_r, tot_l;
+        const int off_s = short_base + block_exclusive_scan(n_short, tmp, &tot_s);
+        const int off_r = row_base + block_exclusive_scan(n_rows, tmp, &tot_r);
+        const int off_l = long_base + block_exclusive_scan(n_long, tmp, &tot_l);
+        if (r.is_short && off_s + n_short <= p.max_short && off_r + n_rows <= p.cap_rows) {
+            int k = off_s;
+            for (int h = 0; h < hkv; ++h) {
+                for (int s = 0; s < ns; ++s, ++k) {
+                    ShortItem it;
+                    it.b = b;
+                    it.h = h;
+                    it.split = s;
+                    it.nsplit = ns;
+                    it.stage_begin = s * sp;
+                    it.stage_end = min((s + 1) * sp, r.stages);
+                    it.partial_base = (ns > 1) ? off_r + (h * ns + s) * R : 0;
+                    it.pad = 0;
+                    p.short_items[k] = it;
+                }
+            }
+        } else if (r.is_short) {
+            s_overflow = 1;
+        }
+        if (r.qtiles > 0 && off_l + n_long <= p.max_long) {
+            int k = off_l;
+            // later query tiles see more keys: emit them first
+            for (int qt = r.qtiles - 1; qt >= 0; --qt) {
+                const int nvalid = min(p.q_tile_tokens, r.n - qt * p.q_tile_tokens);
+                const int kend = min(r.len, r.ctx + qt * p.q_tile_tokens + nvalid);
+                for (int h = 0; h < hkv; ++h, ++k) {
+                    LongItem it;
+                    it.b = b;
+                    it.h = h;
+                    it.q_tile = qt;
+                    it.split = 0;
+                    it.nsplit = 1;
+                    it.key_begin = 0;
+                    it.key_end = kend;
+                    it.partial_base = 0;
+                    p.long_items[k] = it;
+                }
+            }
+        } else if (r.qtiles > 0) {
+            s_overflow = 1;
+        }
+        short_base += tot_s;
+        row_base += tot_r;
+        long_base += tot_l;
+    }
+
+    // 4. counters and header ----------------------------------------------------
+    for (int i = tid; i < p.num_counters; i += kPlanThreads) p.counters[i] = 0;
+    __syncthreads();
+    if (tid == 0) {
+        // A work list that did not fit is never run partially: no items at all.
+        if (s_overflow) flag_status(p.status, PA_DEV_PLAN_OVERFLOW);
+        p.hdr->num_short_items = s_overflow ? 0 : short_base;
+        p.hdr->num_long_items = s_overflow ? 0 : long_base;
+        p.hdr->short_next = 0;
+        p.hdr->long_next = 0;
+        p.hdr->split_stages = sp;
+        p.hdr->partial_rows = row_base;
+    }
+}
+
+int launch_plan(const PlanParams &p, cudaStream_t s) {
+    plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa

@@ -1,0 +1,594 @@
+// pa_short.cu -- split-KV attention for short query rows: decode (q_len 1),
+// speculative verify (q_len 1 + k) and small chunks, i.e. every request whose
+// q_len * group fits 64 rows.  This is the memory-bound half of the step
+// ("11. 推理加速(一):vLLM 原理", §11.3: decode is memory-bound; "PagedAttention
+// (with_kvcache)").
+//
+// Design (one persistent CTA per SM slot, 5 warps):
+//  * warp 4 is the producer: it pulls work items (request b, kv head h, key
+//    range) from a device counter, reads the block table 32 chunks at a time
+//    and issues TMA tensor loads (128-byte swizzled boxes of 16 keys x 64
+//    dims) of K and V into a 3-deep ring of 64-key stages.  The ring keeps
+//    running across item boundaries.
+//  * warps 0-3 consume: for each 16-key chunk, S = Q K^T and O += P V on
+//    mma.sync (bf16 in, fp32 accumulate) with an online softmax in the
+//    log2 domain.  All g query heads of a kv head (and all q_len rows) are
+//    rows of one 16..64-row tile, so every K/V byte is loaded once for the
+//    whole GQA group.  With <= 16 rows the four warps split each stage's keys
+//    and merge their states at the end of the item through the stage buffer.
+//  * split-KV: a long sequence is cut into several items; each writes a
+//    partial (o, lse) state, and the last item to finish (device counter)
+//    folds them with the merge operator (2048ai.net page on the vLLM V1
+//    engine, §02.1 级联推理) -- the fused split-KV epilogue.  A cascade prefix
+//    state can be folded in the same epilogue.
+#include "pa_internal.cuh"
+
+namespace pa {
+
+namespace {
+
+template <int D>
+struct ShortGeom {
+    static constexpr int kHalves = D / 64;                    // 64-dim TMA boxes per row
+    static constexpr int kBoxBytes = kChunkKeys * 128;        // 16 rows x 128 B
+    static constexpr int kChunkBytes = kHalves * kBoxBytes;   // one 16-key chunk of K (or V)
+    static constexpr int kStageBytes = 2 * kStageChunks * kChunkBytes;
+    static constexpr int kCtlBytes = 256;
+    static constexpr int kSmemBytes = kShortStages * kStageBytes + kCtlBytes + 1024;
+    // merge scratch (per writer warp): 16 rows x D floats + 16 m + 16 l
+    static constexpr int kScratchFloats = 16 * D + 32;
+    static_assert(3 * kScratchFloats * 4 <= kStageBytes, "merge scratch must fit one stage");
+};
+
+struct StageMeta {
+    int item, stage, flags, pad;
+};
+constexpr int kFirst = 1, kLast = 2;
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: lazy max update
+
+__device__ __forceinline__ float quad_max(float v) {
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+    return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+}
+__device__ __forceinline__ float quad_sum(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    return v + __shfl_xor_sync(0xffffffffu, v, 2);
+}
+
+// Keep the lower / upper bf16 of a packed pair.
+__device__ __forceinline__ uint32_t keep_pair(uint32_t v, bool lo, bool hi) {
+    return (lo ? (v & 0xFFFFu) : 0u) | (hi ? (v & 0xFFFF0000u) : 0u);
+}
+
+template <int D>
+struct Consumer {
+    using G = ShortGeom<D>;
+    static constexpr int NT = D / 8;   // 8-wide output column tiles
+    static constexpr int KS = D / 16;  // 16-deep k steps over the head dim
+
+    // item-wide
+    int b, h, tok0, ctx, key_end, R, KQ, rt, kq, nsplit, split, partial_base;
+    bool active;
+    // per thread: rows g and g+8 of this warp's 16-row tile
+    int limit0, limit1;
+    uint32_t qa[KS][4];
+    float o[NT][4];
+    float m0, m1, l0, l1;
+};
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(kShortThreads, 2)
+    short_kernel(const ShortParams p, const __grid_constant__ CUtensorMap tmk,
+                 const __grid_constant__ CUtensorMap tmv) {
+    using G = ShortGeom<D>;
+    constexpr int NT = D / 8, KS = D / 16;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *stage_mem = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kShortStages * G::kStageBytes);
+    uint64_t *empty = full + kShortStages;
+    StageMeta *meta = reinterpret_cast<StageMeta *>(empty + kShortStages);
+    int *ctl = reinterpret_cast<int *>(meta + kShortStages);
+    volatile int *abort_flag = ctl;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kShortStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kShortConsumerWarps);
+        }
+        ctl[0] = 0;
+        ctl[1] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto k_box = [&](int slot, int c, int hf) -> uint8_t * {
+        return stage_mem + slot * G::kStageBytes + (c * G::kHalves + hf) * G::kBoxBytes;
+    };
+    auto v_box = [&](int slot, int c, int hf) -> uint8_t * {
+        return stage_mem + slot * G::kStageBytes + kStageChunks * G::kChunkBytes +
+               (c * G::kHalves + hf) * G::kBoxBytes;
+    };
+
+    const int num_items = *reinterpret_cast<volatile int *>(&p.hdr->num_short_items);
+
+    if (warp == kShortConsumerWarps) {
+        // ============================ producer ============================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+        }
+        uint32_t it = 0;
+        bool aborted = false;
+        while (!aborted) {
+            int item_idx = 0;
+            if (lane == 0) item_idx = atomicAdd(&p.hdr->short_next, 1);
+            item_idx = __shfl_sync(0xffffffffu, item_idx, 0);
+            if (item_idx >= num_items) {
+                const int slot = it % kShortStages;
+                bool ok = true;
+                if (lane == 0) {
+                    if (it >= kShortStages)
+                        ok = mbar_wait(&empty[slot], ((it / kShortStages) - 1) & 1, abort_flag);
+                    if (ok) {
+                        meta[slot].item = -1;
+                        mbar_arrive(&full[slot]);
+                    }
+                }
+                __syncwarp();
+                break;
+            }
+            const ShortItem item = p.items[item_idx];
+            const int L = __ldg(p.seq_lens + item.b);
+            const int key_end = min(item.stage_end * kStageKeys, L);
+            const int *bt = p.block_tables + static_cast<int64_t>(item.b) * p.bt_stride;
+            int my_blk = -1;
+            for (int st = item.stage_begin; st < item.stage_end; ++st, ++it) {
+                const int rel = st - item.stage_begin;
+                if ((rel & 7) == 0) {
+                    // block ids of the next 32 chunks (8 stages), one per lane
+                    const int key0 = (st * kStageChunks + lane) * kChunkKeys;
+                    my_blk = -1;
+                    if (key0 < key_end) {
+                        int col = key0 / p.block_size;
+                        if (col >= p.bt_stride) {  // seq_len beyond the table row
+                            flag_status(p.status, PA_DEV_BAD_METADATA);
+                            col = p.bt_stride - 1;
+                        }
+                        int blk = __ldg(bt + col);
+                        if (blk < 0 || blk >= p.num_blocks) {
+                            flag_status(p.status, PA_DEV_BAD_BLOCK);
+                            blk = min(max(blk, 0), p.num_blocks - 1);
+                        }
+                        my_blk = blk;
+                    }
+                }
+                int blks[kStageChunks];
+#pragma unroll
+                for (int c = 0; c < kStageChunks; ++c)
+                    blks[c] = __shfl_sync(0xffffffffu, my_blk, (rel & 7) * kStageChunks + c);
+                const int slot = it % kShortStages;
+                int ok = 1;
+                if (lane == 0 && it >= kShortStages)
+                    ok = mbar_wait(&empty[slot], ((it / kShortStages) - 1) & 1, abort_flag);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) {
+                    aborted = true;
+                    break;
+                }
+                if (lane == 0) {
+                    int nvalid = 0;
+#pragma unroll
+                    for (int c = 0; c < kStageChunks; ++c) nvalid += blks[c] >= 0;
+                    StageMeta mm;
+                    mm.item = item_idx;
+                    mm.stage = st;
+                    mm.flags = (st == item.stage_begin ? kFirst : 0) |
+                               (st == item.stage_end - 1 ? kLast : 0);
+                    mm.pad = 0;
+                    meta[slot] = mm;
+                    mbar_arrive_expect_tx(&full[slot],
+                                          static_cast<uint32_t>(nvalid * 2 * G::kChunkBytes));
+#pragma unroll
+                    for (int c = 0; c < kStageChunks; ++c) {
+                        if (blks[c] < 0) continue;
+                        const int key0 = (st * kStageChunks + c) * kChunkKeys;
+                        const int row = (blks[c] * p.num_kv_heads + item.h) * p.block_size +
+                                        key0 % p.block_size;
+#pragma unroll
+                        for (int hf = 0; hf < G::kHalves; ++hf) {
+                            tma_load_2d(k_box(slot, c, hf), &tmk, hf * 64, row, &full[slot]);
+                            tma_load_2d(v_box(slot, c, hf), &tmv, hf * 64, row, &full[slot]);
+                        }
+                    }
+                }
+                __syncwarp();
+            }
+        }
+        if (aborted && lane == 0) {
+            flag_status(p.status, PA_DEV_WAIT_TIMEOUT);
+            // let copies already in flight land before the CTA exits
+            for (uint32_t k = (it > kShortStages ? it - kShortStages : 0); k < it; ++k)
+                mbar_drain(&full[k % kShortStages], (k / kShortStages) & 1);
+        }
+        return;
+    }
+
+    // ============================ consumers ============================
+    const int g = lane >> 2, t = lane & 3;
+    Consumer<D> cs;
+    cs.active = false;
+    uint32_t it = 0;
+    while (true) {
+        const int slot = it % kShortStages;
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(&full[slot], (it / kShortStages) & 1, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+            if (lane == 0) flag_status(p.status, PA_DEV_WAIT_TIMEOUT);
+            break;
+        }
+        const StageMeta mm = meta[slot];
+        if (mm.item < 0) break;
+
+        if (mm.flags & kFirst) {
+            // ---- item setup ----
+            const ShortItem item = p.items[mm.item];
+            cs.b = item.b;
+            cs.h = item.h;
+            cs.split = item.split;
+            cs.nsplit = item.nsplit;
+            cs.partial_base = item.partial_base;
+            cs.tok0 = __ldg(p.qsl + item.b);
+            const int n = __ldg(p.qsl + item.b + 1) - cs.tok0;
+            cs.ctx = __ldg(p.ctx + item.b);
+            const int L = __ldg(p.seq_lens + item.b);
+            cs.key_end = min(item.stage_end * kStageKeys, L);
+            cs.R = n * p.group;
+            const int RT = (cs.R + 15) >> 4;
+            const int RTp = RT >= 3 ? 4 : RT;
+            cs.KQ = kShortConsumerWarps / RTp;
+            cs.rt = warp / cs.KQ;
+            cs.kq = warp % cs.KQ;
+            cs.active = cs.rt < RT;
+            const int r0 = cs.rt * 16 + g, r1 = r0 + 8;
+            cs.limit0 = r0 < cs.R ? cs.ctx + r0 / p.group : -1;
+            cs.limit1 = r1 < cs.R ? cs.ctx + r1 / p.group : -1;
+            if (cs.active) {
+                const uint32_t *q0 = nullptr, *q1 = nullptr;
+                if (r0 < cs.R)
+                    q0 = reinterpret_cast<const uint32_t *>(
+                        p.q + (static_cast<int64_t>(cs.tok0 + r0 / p.group) * p.num_q_heads +
+                               cs.h * p.group + r0 % p.group) *
+                                  D);
+                if (r1 < cs.R)
+                    q1 = reinterpret_cast<const uint32_t *>(
+                        p.q + (static_cast<int64_t>(cs.tok0 + r1 / p.group) * p.num_q_heads +
+                               cs.h * p.group + r1 % p.group) *
+                                  D);
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int w = ks * 8 + t;  // 32-bit word index of dims ks*16 + 2t
+                    cs.qa[ks][0] = q0 ? __ldg(q0 + w) : 0u;
+                    cs.qa[ks][1] = q1 ? __ldg(q1 + w) : 0u;
+                    cs.qa[ks][2] = q0 ? __ldg(q0 + w + 4) : 0u;
+                    cs.qa[ks][3] = q1 ? __ldg(q1 + w + 4) : 0u;
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) cs.o[nt][e] = 0.f;
+            cs.m0 = cs.m1 = -INFINITY;
+            cs.l0 = cs.l1 = 0.f;
+        }
+
+        // ---- process this warp's chunks of the stage ----
+        if (cs.active) {
+            for (int c = cs.kq; c < kStageChunks; c += cs.KQ) {
+                const int key0 = (mm.stage * kStageChunks + c) * kChunkKeys;
+                if (key0 >= cs.key_end) break;
+                const uint32_t kb = smem_u32(k_box(slot, c, 0));
+                const uint32_t vb = smem_u32(v_box(slot, c, 0));
+                const int mi = lane >> 3;
+                float sacc[2][4];
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sacc[i][e] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int key = (mi >> 1) * 8 + (lane & 7);
+                    const int col = (ks & 3) * 2 + (mi & 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kb + (ks >> 2) * G::kBoxBytes + sw128_offset(key, col), b0, b1, b2,
+                            b3);
+                    mma_bf16_16816(sacc[0], cs.qa[ks][0], cs.qa[ks][1], cs.qa[ks][2],
+                                   cs.qa[ks][3], b0, b1);
+                    mma_bf16_16816(sacc[1], cs.qa[ks][0], cs.qa[ks][1], cs.qa[ks][2],
+                                   cs.qa[ks][3], b2, b3);
+                }
+                // scale to log2 units and mask (causal limit per row, item key range)
+                const bool need_mask = (key0 + kChunkKeys - 1 > cs.ctx) ||
+                                       (key0 + kChunkKeys > cs.key_end);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float s = sacc[nt][e] * p.scale_log2;
+                        if (need_mask) {
+                            const int key = key0 + nt * 8 + 2 * t + (e & 1);
+                            const int lim = (e < 2) ? cs.limit0 : cs.limit1;
+                            if (key > lim || key >= cs.key_end) s = -INFINITY;
+                        }
+                        sacc[nt][e] = s;
+                    }
+                float mx0 = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
+                float mx1 = fmaxf(fmaxf(sacc[0][2], sacc[0][3]), fmaxf(sacc[1][2], sacc[1][3]));
+                mx0 = quad_max(mx0);
+                mx1 = quad_max(mx1);
+                const bool up0 = mx0 > cs.m0 + kRescaleThreshold || (cs.m0 == -INFINITY && mx0 > -INFINITY);
+                const bool up1 = mx1 > cs.m1 + kRescaleThreshold || (cs.m1 == -INFINITY && mx1 > -INFINITY);
+                if (__any_sync(0xffffffffu, up0 || up1)) {
+                    const float nm0 = up0 ? mx0 : cs.m0;
+                    const float nm1 = up1 ? mx1 : cs.m1;
+                    const float a0 = up0 ? (cs.m0 == -INFINITY ? 0.f : exp2f(cs.m0 - nm0)) : 1.f;
+                    const float a1 = up1 ? (cs.m1 == -INFINITY ? 0.f : exp2f(cs.m1 - nm1)) : 1.f;
+                    cs.m0 = nm0;
+                    cs.m1 = nm1;
+                    cs.l0 *= a0;
+                    cs.l1 *= a1;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        cs.o[nt][0] *= a0;
+                        cs.o[nt][1] *= a0;
+                        cs.o[nt][2] *= a1;
+                        cs.o[nt][3] *= a1;
+                    }
+                }
+                const float ref0 = cs.m0 == -INFINITY ? 0.f : cs.m0;
+                const float ref1 = cs.m1 == -INFINITY ? 0.f : cs.m1;
+                float pr[2][4];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    pr[nt][0] = exp2f(sacc[nt][0] - ref0);
+                    pr[nt][1] = exp2f(sacc[nt][1] - ref0);
+                    pr[nt][2] = exp2f(sacc[nt][2] - ref1);
+                    pr[nt][3] = exp2f(sacc[nt][3] - ref1);
+                }
+                cs.l0 += pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
+                cs.l1 += pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
+                const uint32_t pa0 = pack_bf16x2(pr[0][0], pr[0][1]);
+                const uint32_t pa1 = pack_bf16x2(pr[0][2], pr[0][3]);
+                const uint32_t pa2 = pack_bf16x2(pr[1][0], pr[1][1]);
+                const uint32_t pa3 = pack_bf16x2(pr[1][2], pr[1][3]);
+                // V rows past the item's keys may hold anything (even NaN):
+                // zero them in the fragments of a partially valid chunk.
+                const int nvalid = cs.key_end - key0;
+                const bool tail = nvalid < kChunkKeys;
+#pragma unroll
+                for (int dp = 0; dp < KS; ++dp) {
+                    const int key = (mi & 1) * 8 + (lane & 7);
+                    const int col = (dp & 3) * 2 + (mi >> 1);
+                    uint32_t v0, v1, v2, v3;
+                    ldsm_x4_t(vb + (dp >> 2) * G::kBoxBytes + sw128_offset(key, col), v0, v1, v2,
+                              v3);
+                    if (tail) {
+                        const bool k0 = 2 * t < nvalid, k1 = 2 * t + 1 < nvalid;
+                        const bool k8 = 2 * t + 8 < nvalid, k9 = 2 * t + 9 < nvalid;
+                        v0 = keep_pair(v0, k0, k1);
+                        v2 = keep_pair(v2, k0, k1);
+                        v1 = keep_pair(v1, k8, k9);
+                        v3 = keep_pair(v3, k8, k9);
+                    }
+                    mma_bf16_16816(cs.o[2 * dp], pa0, pa1, pa2, pa3, v0, v1);
+                    mma_bf16_16816(cs.o[2 * dp + 1], pa0, pa1, pa2, pa3, v2, v3);
+                }
+            }
+        }
+
+        bool wrote_stage = false;
+        if (mm.flags & kLast) {
+            // ---- item epilogue ----
+            float l0 = quad_sum(cs.l0), l1 = quad_sum(cs.l1);
+            if (cs.KQ > 1) {
+                // merge the KQ warps that share a row tile, through this stage's buffer
+                named_bar_sync(1, 32 * kShortConsumerWarps);
+                float *scratch = reinterpret_cast<float *>(stage_mem + slot * G::kStageBytes);
+                wrote_stage = true;
+                if (cs.active && cs.kq > 0) {
+                    float *reg = scratch + (cs.rt * (cs.KQ - 1) + cs.kq - 1) * G::kScratchFloats;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        *reinterpret_cast<float2 *>(reg + g * D + nt * 8 + 2 * t) =
+                            make_float2(cs.o[nt][0], cs.o[nt][1]);
+                        *reinterpret_cast<float2 *>(reg + (g + 8) * D + nt * 8 + 2 * t) =
+                            make_float2(cs.o[nt][2], cs.o[nt][3]);
+                    }
+                    if (t == 0) {
+                        reg[16 * D + g] = cs.m0;
+                        reg[16 * D + g + 8] = cs.m1;
+                        reg[16 * D + 16 + g] = l0;
+                        reg[16 * D + 16 + g + 8] = l1;
+                    }
+                }
+                named_bar_sync(1, 32 * kShortConsumerWarps);
+                if (cs.active && cs.kq == 0) {
+                    for (int k = 1; k < cs.KQ; ++k) {
+                        const float *reg = scratch + (cs.rt * (cs.KQ - 1) + k - 1) * G::kScratchFloats;
+                        const float om0 = reg[16 * D + g], om1 = reg[16 * D + g + 8];
+                        const float ol0 = reg[16 * D + 16 + g], ol1 = reg[16 * D + 16 + g + 8];
+                        const float M0 = fmaxf(cs.m0, om0), M1 = fmaxf(cs.m1, om1);
+                        const float a0 = cs.m0 == -INFINITY ? 0.f : exp2f(cs.m0 - M0);
+                        const float b0 = om0 == -INFINITY ? 0.f : exp2f(om0 - M0);
+                        const float a1 = cs.m1 == -INFINITY ? 0.f : exp2f(cs.m1 - M1);
+                        const float b1 = om1 == -INFINITY ? 0.f : exp2f(om1 - M1);
+                        l0 = a0 * l0 + b0 * ol0;
+                        l1 = a1 * l1 + b1 * ol1;
+                        cs.m0 = M0;
+                        cs.m1 = M1;
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const float2 x = *reinterpret_cast<const float2 *>(reg + g * D + nt * 8 + 2 * t);
+                            const float2 y = *reinterpret_cast<const float2 *>(reg + (g + 8) * D + nt * 8 + 2 * t);
+                            cs.o[nt][0] = a0 * cs.o[nt][0] + b0 * x.x;
+                            cs.o[nt][1] = a0 * cs.o[nt][1] + b0 * x.y;
+                            cs.o[nt][2] = a1 * cs.o[nt][2] + b1 * y.x;
+                            cs.o[nt][3] = a1 * cs.o[nt][3] + b1 * y.y;
+                        }
+                    }
+                }
+            }
+            if (cs.active && cs.kq == 0) {
+                // final state of rows r0 = rt*16+g and r1 = r0+8 over this item's keys
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int r = cs.rt * 16 + g + half * 8;
+                    if (r >= cs.R) continue;
+                    const float l = half ? l1 : l0;
+                    const float m = half ? cs.m1 : cs.m0;
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    const float lse_v = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+                    const int tok = cs.tok0 + r / p.group;
+                    const int hq = cs.h * p.group + r % p.group;
+                    const int64_t row = static_cast<int64_t>(tok) * p.num_q_heads + hq;
+                    if (cs.nsplit == 1) {
+                        float wa = 1.f, wb = 0.f, lse_f = lse_v;
+                        const float *xo = nullptr;
+                        if (p.extra_o) {
+                            const float xl = __ldg(p.extra_lse + row);
+                            const float M = fmaxf(lse_v, xl);
+                            if (M == -INFINITY) {
+                                wa = 0.f;
+                            } else {
+                                const float ea = __expf(lse_v - M), eb = __expf(xl - M);
+                                wa = ea / (ea + eb);
+                                wb = eb / (ea + eb);
+                                lse_f = M + __logf(ea + eb);
+                                xo = p.extra_o + row * D;
+                            }
+                        }
+                        uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + row * D);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            float x = cs.o[nt][half * 2] * inv, y = cs.o[nt][half * 2 + 1] * inv;
+                            if (p.extra_o) {
+                                x *= wa;
+                                y *= wa;
+                                if (xo) {
+                                    const float2 e2 = __ldg(reinterpret_cast<const float2 *>(xo + nt * 8 + 2 * t));
+                                    x += wb * e2.x;
+                                    y += wb * e2.y;
+                                }
+                            }
+                            dst[(nt * 8 + 2 * t) >> 1] = pack_bf16x2(x, y);
+                        }
+                        if (p.lse && t == 0) p.lse[row] = lse_f;
+                    } else {
+                        float *dst = p.partial_o + static_cast<int64_t>(cs.partial_base + r) * D;
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            __stcg(reinterpret_cast<float2 *>(dst + nt * 8 + 2 * t),
+                                   make_float2(cs.o[nt][half * 2] * inv, cs.o[nt][half * 2 + 1] * inv));
+                        if (t == 0) __stcg(p.partial_lse + cs.partial_base + r, lse_v);
+                    }
+                }
+            }
+            if (cs.nsplit > 1) {
+                // fused split-KV epilogue: the last split of (b, h) folds all partials
+                __threadfence();
+                named_bar_sync(1, 32 * kShortConsumerWarps);
+                if (threadIdx.x == 0) {
+                    const int old = atomicAdd(p.counters + cs.b * p.num_kv_heads + cs.h, 1);
+                    ctl[1] = (old == cs.nsplit - 1) ? 1 : 0;
+                }
+                named_bar_sync(1, 32 * kShortConsumerWarps);
+                if (ctl[1]) {
+                    __threadfence();
+                    const int base = cs.partial_base - cs.split * cs.R;
+                    const int total = cs.R * D;
+                    for (int idx = threadIdx.x; idx < total; idx += 32 * kShortConsumerWarps) {
+                        const int r = idx / D, e = idx - r * D;
+                        const int tok = cs.tok0 + r / p.group;
+                        const int hq = cs.h * p.group + r % p.group;
+                        const int64_t row = static_cast<int64_t>(tok) * p.num_q_heads + hq;
+                        const float xl = p.extra_o ? __ldg(p.extra_lse + row) : -INFINITY;
+                        const float M = lse_max_of(p.partial_lse + base + r, cs.R, cs.nsplit, xl);
+                        float acc = 0.f, wsum = 0.f;
+                        if (M != -INFINITY) {
+                            for (int s = 0; s < cs.nsplit; ++s) {
+                                const float ls = __ldcg(p.partial_lse + base + s * cs.R + r);
+                                const float w = __expf(ls - M);
+                                wsum += w;
+                                acc += w * __ldcg(p.partial_o + static_cast<int64_t>(base + s * cs.R + r) * D + e);
+                            }
+                            if (p.extra_o) {
+                                const float w = __expf(xl - M);
+                                wsum += w;
+                                acc += w * __ldg(p.extra_o + row * D + e);
+                            }
+                        }
+                        const float val = wsum > 0.f ? acc / wsum : 0.f;
+                        p.out[row * D + e] = __float2bfloat16_rn(val);
+                        if (e == 0 && p.lse) p.lse[row] = wsum > 0.f ? M + __logf(wsum) : -INFINITY;
+                    }
+                }
+                named_bar_sync(1, 32 * kShortConsumerWarps);
+            }
+        }
+        if (wrote_stage) fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        ++it;
+    }
+}
+
+size_t short_smem_bytes(int head_dim) {
+    return head_dim == 128 ? ShortGeom<128>::kSmemBytes : ShortGeom<64>::kSmemBytes;
+}
+
+template <int D>
+static int configure_short() {
+    static bool done = false;  // per process; attribute is per function, device-independent
+    if (!done) {
+        if (cudaFuncSetAttribute(short_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 ShortGeom<D>::kSmemBytes) != cudaSuccess)
+            return PA_ERR_CUDA;
+        done = true;
+    }
+    return PA_OK;
+}
+
+int short_max_ctas_per_sm(int head_dim) {
+    int n = 0;
+    if (head_dim == 128) {
+        if (configure_short<128>() != PA_OK) return 1;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, short_kernel<128>, kShortThreads,
+                                                      ShortGeom<128>::kSmemBytes);
+    } else {
+        if (configure_short<64>() != PA_OK) return 1;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, short_kernel<64>, kShortThreads,
+                                                      ShortGeom<64>::kSmemBytes);
+    }
+    return n > 0 ? n : 1;
+}
+
+int launch_short(const ShortParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                 int head_dim, int grid, cudaStream_t s) {
+    if (grid <= 0) return PA_OK;
+    if (head_dim == 128) {
+        if (configure_short<128>() != PA_OK) return PA_ERR_CUDA;
+        short_kernel<128><<<grid, kShortThreads, ShortGeom<128>::kSmemBytes, s>>>(p, tk, tv);
+    } else {
+        if (configure_short<64>() != PA_OK) return PA_ERR_CUDA;
+        short_kernel<64><<<grid, kShortThreads, ShortGeom<64>::kSmemBytes, s>>>(p, tk, tv);
+    }
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa

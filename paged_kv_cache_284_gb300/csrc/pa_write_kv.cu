@@ -1,0 +1,52 @@
+// pa_write_kv.cu -- reshape_and_cache: scatter this step's K/V rows into
+// their cache slots ("11. 推理加速(一):vLLM 原理", §11.2: tokens fill
+// fixed-size physical blocks; slot = block * block_size + offset).
+//
+// Pure HBM copy: each thread moves one 16-byte piece of one (token, kv head)
+// row for K and the same piece for V, so a warp covers 512 contiguous bytes
+// of the source and whole 16-byte sectors of the destination row.
+#include "pa_internal.cuh"
+
+namespace pa {
+
+__global__ void __launch_bounds__(256) write_kv_kernel(
+    const uint4 *__restrict__ k, const uint4 *__restrict__ v, const int64_t *__restrict__ slots,
+    int num_tokens, int num_kv_heads, int pieces_per_row, int block_size, int num_blocks,
+    uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, unsigned *status) {
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t per_token = static_cast<int64_t>(num_kv_heads) * pieces_per_row;
+    if (idx >= per_token * num_tokens) return;
+    const int64_t t = idx / per_token;
+    const int64_t rem = idx - t * per_token;  // = h * pieces_per_row + piece
+    const int64_t s = __ldg(slots + t);
+    if (s < 0) return;  // padding token
+    const int64_t blk = s / block_size;
+    const int64_t off = s - blk * block_size;
+    if (blk >= num_blocks) {
+        flag_status(status, PA_DEV_BAD_SLOT);
+        return;
+    }
+    const int64_t h = rem / pieces_per_row;
+    const int64_t piece = rem - h * pieces_per_row;
+    const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * pieces_per_row + piece;
+    const uint4 kv_k = __ldg(k + idx);
+    const uint4 kv_v = __ldg(v + idx);
+    k_cache[dst] = kv_k;
+    v_cache[dst] = kv_v;
+}
+
+int launch_write_kv(const void *k, const void *v, const int64_t *slots, int num_tokens,
+                    const pa_kv_desc *kv, unsigned *status, cudaStream_t s) {
+    if (num_tokens == 0) return PA_OK;
+    const int pieces = kv->head_dim * 2 / 16;
+    const int64_t total = static_cast<int64_t>(num_tokens) * kv->num_kv_heads * pieces;
+    const int threads = 256;
+    const int64_t blocks = (total + threads - 1) / threads;
+    write_kv_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slots, num_tokens,
+        kv->num_kv_heads, pieces, kv->block_size, kv->num_blocks,
+        static_cast<uint4 *>(kv->k_cache), static_cast<uint4 *>(kv->v_cache), status);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa
