@@ -194,6 +194,19 @@ def tensor_core_flops(step, reqs):
     return total
 
 
+def make_events(n):
+    """n (start, end) timing events, created now: torch creates the CUDA
+    event lazily at the first record, and the library records them by
+    handle, so each is recorded once here, outside any timed region."""
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(n)]
+    for a, b in pairs:
+        a.record()
+        b.record()
+    torch.cuda.synchronize()
+    return pairs
+
+
 def time_steps(fn, steps, stream):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -297,7 +310,13 @@ def run_ours(args):
 
     # ---- headline: the mixed step ------------------------------------------
     t0 = time.time()
-    pool, (step,) = workloads.mixed_step(seed=workloads.SEED_BASE + 3 + 1000 * rank)
+    if args.workload == "mixed_step":
+        pool, (step,) = workloads.mixed_step(seed=workloads.SEED_BASE + 3 + 1000 * rank)
+    elif args.workload == "decode_heavy":
+        pool, (step,) = workloads.decode_heavy(seed=workloads.SEED_BASE + 2 + 1000 * rank)
+    else:  # the 8 prefill chunks of the mixed step alone
+        pool, (step,) = workloads.mixed_step(seed=workloads.SEED_BASE + 3 + 1000 * rank,
+                                             num_decode=0, num_spec=0)
     log(f"[bench] mixed step generated in {time.time() - t0:.1f}s: "
         f"{step.num_seqs} requests, {step.num_q_tokens} tokens, {pool.num_blocks} blocks")
     ds = DeviceStep(pool, step, dev)
@@ -314,7 +333,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     t_w = time.time()
     n_w = 0
-    while n_w < args.warmup or time.time() - t_w < 0.5:
+    while n_w < args.warmup or time.time() - t_w < args.min_warmup_s:
         ds.run()
         n_w += 1
         if n_w % 20 == 0:
@@ -322,9 +341,7 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     # timed region: exactly K steps, kernel events for the two attention kernels
-    ev = {w: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)] for w in (pk.PA_KERNEL_SPLIT_KV,
-                                                     pk.PA_KERNEL_TENSOR_CORE)}
+    ev = {w: make_events(args.steps) for w in (pk.PA_KERNEL_SPLIT_KV, pk.PA_KERNEL_TENSOR_CORE)}
     it = [0]
 
     def timed_step():
@@ -354,7 +371,7 @@ def run_ours(args):
     value = world * step.num_q_tokens * args.steps / (ms / 1000.0)
     short_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[pk.PA_KERNEL_SPLIT_KV])
     long_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[pk.PA_KERNEL_TENSOR_CORE])
-    achieved = short_bytes / (short_ms / 1000.0) / 1e9
+    achieved = short_bytes / (short_ms / 1000.0) / 1e9 if short_bytes else 0.0
     tr = traffic_for("split_kv_mixed_step")
     traffic = None
     if tr:
@@ -364,7 +381,7 @@ def run_ours(args):
                 "kernel": "split-KV decode/short-q kernel (pa_short.cu)",
                 "kernel_ms": short_ms, "algorithmic_bytes": short_bytes,
                 "peak_source": f"{peak_src} hbm_gbs (copy)"}
-    tflops = long_flops / (long_ms / 1000.0) / 1e12
+    tflops = long_flops / (long_ms / 1000.0) / 1e12 if long_flops else 0.0
     tensor_core = {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
                    "frac": tflops / tc_peak, "kernel": "tcgen05 prefill kernel (pa_long.cu)",
                    "kernel_ms": long_ms, "flops": long_flops,
@@ -435,7 +452,8 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "requests": step.num_seqs,
+            "config": {"workload": WORKLOAD if args.workload == "mixed_step" else step.label,
+                       "requests": step.num_seqs,
                        "query_tokens": step.num_q_tokens, "pool_blocks": pool.num_blocks,
                        "kv_bytes_read_per_step": kv_bytes(step, range(step.num_seqs)),
                        "l2": "inputs larger than L2 (no flush needed)",
@@ -465,8 +483,7 @@ def bench_decode_heavy(args, dev, hbm_peak):
     for _ in range(max(3, args.warmup)):
         ds.run(write=False)
     torch.cuda.synchronize()
-    s_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(args.steps)]
+    s_ev = make_events(args.steps)
     it = [0]
 
     def one():
@@ -538,6 +555,12 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--workload", choices=["mixed_step", "decode_heavy", "prefill"],
+                    default="mixed_step",
+                    help="headline workload (mixed_step is the benchmark; the others are "
+                         "single-kernel cases for profiling)")
+    ap.add_argument("--min-warmup-s", type=float, default=0.5,
+                    help="keep warming up at least this long (clock samples need a busy GPU)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
