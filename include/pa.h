@@ -158,6 +158,30 @@ int pa_merge_states(const void *o_a, const float *lse_a, const void *o_b, const 
                     void *stream);
 
 /*
+ * pa_attention for callers that cannot allocate device memory (no
+ * counterpart on the pages: this is a deployment convenience).  Same
+ * arguments and results as pa_attention, without the workspace: the
+ * library keeps its scratch (work list, split partial states, counters) in
+ * one fixed device array of PA_NO_ALLOC_SCRATCH_BYTES that every GPU which
+ * loads the library holds until the process exits.  The call allocates
+ * nothing and frees nothing.
+ *  - The first call on each device looks up the array's device address
+ *    (with that device current); make it before any stream capture.
+ *  - All calls on a device share the array and it keeps the last call's
+ *    contents: calls whose kernels overlap on the GPU race and give wrong
+ *    results.  Order them (one stream, or events).
+ *  - A step whose work list does not fit returns PA_ERR_WORKSPACE with a
+ *    message; when little room is left for split-KV partial states the
+ *    planner simply uses longer splits.
+ */
+#define PA_NO_ALLOC_SCRATCH_BYTES (32u << 20)
+int pa_attention_no_alloc(const void *q, const pa_kv_desc *kv, const int32_t *block_tables,
+                          int32_t max_blocks_per_seq, const int32_t *query_start_loc,
+                          const int32_t *context_lens, const int32_t *seq_lens,
+                          int32_t num_seqs, int32_t num_q_tokens, int32_t num_q_heads,
+                          float scale, void *out, float *lse, void *stream);
+
+/*
  * Workspace bytes for pa_prefix_attention / pa_cascade_decode.
  */
 size_t pa_cascade_workspace_size(int32_t num_seqs, int32_t num_q_tokens, int32_t num_q_heads,

@@ -34,7 +34,8 @@ PA_DEV_BAD_METADATA, PA_DEV_BAD_BLOCK, PA_DEV_BAD_SLOT, PA_DEV_WAIT_TIMEOUT, \
 EXPORTED = ["pa_write_kv", "pa_attention_workspace_size", "pa_attention", "pa_attention_ex",
             "pa_merge_states", "pa_cascade_workspace_size", "pa_prefix_attention",
             "pa_cascade_decode", "pa_validate_metadata", "pa_last_error_message",
-            "pa_status_string", "pa_read_device_status", "pa_set_profile_events"]
+            "pa_status_string", "pa_read_device_status", "pa_set_profile_events",
+            "pa_attention_no_alloc"]
 PA_KERNEL_WRITE_KV, PA_KERNEL_PLAN, PA_KERNEL_SPLIT_KV, PA_KERNEL_TENSOR_CORE = range(4)
 
 
@@ -75,6 +76,8 @@ def _declare(lib):
         "pa_read_device_status": ([ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, P],
                                   ctypes.c_int),
         "pa_set_profile_events": ([i32, P, P], ctypes.c_int),
+        "pa_attention_no_alloc": ([P, KV, P, i32, P, P, P, i32, i32, i32, f32, P, P, P],
+                                  ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -265,3 +268,24 @@ def set_profile_events(which: int, start=None, end=None):
     s = None if start is None else ctypes.c_void_p(start.cuda_event)
     e = None if end is None else ctypes.c_void_p(end.cuda_event)
     _check(lib().pa_set_profile_events(int(which), s, e), "pa_set_profile_events")
+
+
+def pa_attention_no_alloc(q, k_cache, v_cache, block_tables, query_start_loc, context_lens,
+                          seq_lens, scale, out, lse=None, stream=None):
+    """pa_attention without a workspace, for callers that cannot allocate
+    device memory: the library's own fixed scratch array is used.  Calls that
+    overlap on the GPU share that array and must be ordered."""
+    _need(q, "q", torch.bfloat16)
+    _need(out, "out", torch.bfloat16)
+    for name, t in (("block_tables", block_tables), ("query_start_loc", query_start_loc),
+                    ("context_lens", context_lens), ("seq_lens", seq_lens)):
+        _need(t, name, torch.int32)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    kv = kv_desc(k_cache, v_cache)
+    T, hq, _ = q.shape
+    _check(lib().pa_attention_no_alloc(_ptr(q), ctypes.byref(kv), _ptr(block_tables),
+                                       int(block_tables.shape[1]), _ptr(query_start_loc),
+                                       _ptr(context_lens), _ptr(seq_lens), int(seq_lens.shape[0]),
+                                       T, hq, float(scale), _ptr(out), _ptr(lse), _stream(stream)),
+           "pa_attention_no_alloc")

@@ -415,6 +415,69 @@ int prefix_partial_rows(int T, int prefix_len, int num_kv_heads, int group) {
 
 }  // namespace
 
+namespace pa {
+
+// Attention for one step inside a caller-provided scratch region of fixed
+// size (used by the entry point that never allocates).  The work lists get
+// the smallest capacity that always fits (one split per request and kv
+// head, plus room for extra splits); whatever space is left holds split-KV
+// partial states, and the planner picks split sizes that fit it.
+int attention_in_fixed_workspace(const void *q, const pa_kv_desc *kv,
+                                 const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t *query_start_loc, const int32_t *context_lens,
+                                 const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_tokens,
+                                 int32_t num_q_heads, float scale, void *out, float *lse,
+                                 void *scratch, size_t scratch_bytes, cudaStream_t s) {
+    g_err[0] = 0;
+    int rc = common_checks(q, kv, num_q_tokens, num_q_heads, scale, out, scratch);
+    if (rc != PA_OK) return rc;
+    if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs < 0");
+    if (num_seqs == 0 || num_q_tokens == 0) return PA_OK;
+    if (!block_tables || !query_start_loc || !context_lens || !seq_lens)
+        return fail(PA_ERR_INVALID_ARG, "metadata pointer is NULL");
+    if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq <= 0");
+    const int hkv = kv->num_kv_heads, D = kv->head_dim;
+    const int tq = q_tile_tokens(num_q_heads / hkv);
+    WsLayout L{};
+    L.max_short = hkv * num_seqs + 4096;
+    L.max_long = hkv * ((num_q_tokens + tq - 1) / tq + num_seqs);
+    L.num_counters = hkv * num_seqs;
+    size_t off = 0;
+    L.header = off;
+    off = align256(off + sizeof(PlanHeader));
+    L.counters = off;
+    off = align256(off + sizeof(int) * static_cast<size_t>(L.num_counters));
+    L.short_items = off;
+    off = align256(off + sizeof(ShortItem) * static_cast<size_t>(L.max_short));
+    L.long_items = off;
+    off = align256(off + sizeof(LongItem) * static_cast<size_t>(L.max_long));
+    const size_t fixed = off + 512;  // + alignment of the two partial arrays
+    if (fixed > scratch_bytes)
+        return fail(PA_ERR_WORKSPACE,
+                    "step too large for the fixed scratch: its work lists need %zu bytes, "
+                    "the scratch holds %zu", fixed, scratch_bytes);
+    const size_t rows = (scratch_bytes - fixed) / (sizeof(float) * (static_cast<size_t>(D) + 1));
+    L.cap_rows = static_cast<int>(std::min<size_t>(rows, 1u << 24));
+    L.partial_o = off;
+    off = align256(off + sizeof(float) * static_cast<size_t>(L.cap_rows) * D);
+    L.partial_lse = off;
+    off = align256(off + sizeof(float) * static_cast<size_t>(L.cap_rows));
+    L.total = off;
+    if (L.total > scratch_bytes) return fail(PA_ERR_WORKSPACE, "scratch layout overflow");
+    DeviceInfo *dev;
+    if ((rc = device_info(&dev)) != PA_OK) return rc;
+    StepMaps maps;
+    if ((rc = make_maps(&maps, q, kv, num_q_tokens, num_q_heads)) != PA_OK) return rc;
+    return run_step(q, kv, block_tables, max_blocks_per_seq, query_start_loc, context_lens,
+                    seq_lens, num_seqs, num_q_tokens, num_q_heads, scale, out, lse,
+                    static_cast<uint8_t *>(scratch), L, kShortMaxRows, 0, nullptr, nullptr,
+                    false, maps, dev, s);
+}
+
+int set_error_message(int code, const char *msg) { return fail(code, "%s", msg); }
+
+}  // namespace pa
+
 extern "C" {
 
 const char *pa_last_error_message(void) { return g_err; }

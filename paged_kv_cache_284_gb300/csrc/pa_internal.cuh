@@ -133,6 +133,16 @@ int launch_long(const LongParams &p, const CUtensorMap &tq, const CUtensorMap &t
 int launch_merge(const void *oa, const float *la, const void *ob, const float *lb, int n,
                  int heads, int head_dim, void *out, float *lse_out, cudaStream_t s);
 size_t short_smem_bytes(int head_dim);
+// One attention step whose scratch is a caller-provided region of fixed size
+// (defined in pa_api.cu, used by pa_static.cu).
+int attention_in_fixed_workspace(const void *q, const pa_kv_desc *kv,
+                                 const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t *query_start_loc, const int32_t *context_lens,
+                                 const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_tokens,
+                                 int32_t num_q_heads, float scale, void *out, float *lse,
+                                 void *scratch, size_t scratch_bytes, cudaStream_t s);
+// Record `msg` as the calling thread's last error message; returns `code`.
+int set_error_message(int code, const char *msg);
 size_t long_smem_bytes(int head_dim);
 
 // ---------------------------------------------------------------------------
