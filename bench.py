@@ -11,10 +11,12 @@ resident in HBM and larger than L2 (about 3.9 GB of KV is read per step), so
 no L2 flush is needed between steps.
 
 Also reported on the same line:
-  roofline      the split-KV kernel (the step's largest share of time):
-                algorithmic bytes per launch / its CUDA-event duration inside
-                the timed region, against the measured HBM copy bandwidth;
-  tensor_core   the same for the tcgen05 prefill kernel in TFLOP/s;
+  roofline      the attention kernel with the larger share of the step:
+                algorithmic bytes (or flops) per launch / its CUDA-event
+                duration inside the timed region, against the measured HBM
+                copy bandwidth (or bf16 tensor throughput);
+  kernels       both attention kernels in that form (split-KV in GB/s,
+                tcgen05 prefill in TFLOP/s);
   decode_heavy  256 decode rows, seq_len uniform in 512..4096: KV GB/s;
   cascade       64 requests sharing an 8192-token prefix: cascade decode vs
                 plain paged attention over the full tables;
@@ -373,19 +375,22 @@ def run_ours(args):
     long_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[pk.PA_KERNEL_TENSOR_CORE])
     achieved = short_bytes / (short_ms / 1000.0) / 1e9 if short_bytes else 0.0
     tr = traffic_for("split_kv_mixed_step")
-    traffic = None
-    if tr:
-        traffic = tr["dram_bytes_per_algorithmic_byte"] * short_bytes
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "traffic": traffic,
+    split_kv = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak,
+                "traffic": tr["dram_bytes_per_algorithmic_byte"] * short_bytes if tr else None,
                 "kernel": "split-KV decode/short-q kernel (pa_short.cu)",
                 "kernel_ms": short_ms, "algorithmic_bytes": short_bytes,
                 "peak_source": f"{peak_src} hbm_gbs (copy)"}
     tflops = long_flops / (long_ms / 1000.0) / 1e12 if long_flops else 0.0
+    tr = traffic_for("tensor_core_mixed_step")
     tensor_core = {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
-                   "frac": tflops / tc_peak, "kernel": "tcgen05 prefill kernel (pa_long.cu)",
+                   "frac": tflops / tc_peak,
+                   "traffic": tr["dram_bytes_per_flop"] * long_flops if tr else None,
+                   "kernel": "tcgen05 prefill kernel (pa_long.cu)",
                    "kernel_ms": long_ms, "flops": long_flops,
                    "peak_source": f"{peak_src} bf16_tflops (burst)"}
+    # the roofline object describes the kernel with the larger share of the step
+    roofline = split_kv if short_ms >= long_ms else tensor_core
 
     # ---- e2e through the public API with host buffers ----------------------
     e2e = None
@@ -460,7 +465,7 @@ def run_ours(args):
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "seed": workloads.SEED_BASE + 3},
             "roofline": roofline,
-            "tensor_core": tensor_core,
+            "kernels": {"split_kv": split_kv, "tensor_core": tensor_core},
             "decode_heavy": decode,
             "cascade": cascade,
             "cpu_baseline": cpu,

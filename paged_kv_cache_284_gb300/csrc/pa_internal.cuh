@@ -27,7 +27,7 @@ constexpr int kShortConsumerWarps = 4;
 constexpr int kShortThreads = 32 * (kShortConsumerWarps + 1);
 constexpr int kLongRows = 128;        // tcgen05 tile: M = 128 query rows
 constexpr int kLongKeys = 128;        // tcgen05 tile: N = 128 keys per KV tile
-constexpr int kLongThreads = 192;     // 6 warps: TMA, MMA, 4 x softmax
+constexpr int kLongThreads = 224;     // 7 warps: K+Q loads, MMA, 4 x softmax, V loads
 constexpr int kPlanThreads = 1024;
 constexpr int kMinSplitStages = 4;    // 256 keys: smallest automatic split
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s per pipeline wait

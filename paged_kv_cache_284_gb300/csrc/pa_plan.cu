@@ -91,6 +91,17 @@ __device__ __forceinline__ ReqInfo load_req(const PlanParams &p, int b) {
     return r;
 }
 
+constexpr int kSortBins = kPlanThreads;  // bins of the longest-first sort
+
+// Sort bin of query tile qt of a long request: bin 0 holds the most 128-key
+// tiles.
+__device__ __forceinline__ int long_bin(const PlanParams &p, const ReqInfo &r, int qt) {
+    const int nvalid = min(p.q_tile_tokens, r.n - qt * p.q_tile_tokens);
+    const int kend = min(r.len, r.ctx + qt * p.q_tile_tokens + nvalid);
+    const int tiles = (kend + kLongKeys - 1) / kLongKeys;
+    return kSortBins - 1 - min(tiles, kSortBins - 1);
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     __shared__ int tmp[33];
     __shared__ long long tmpl[33];
@@ -155,11 +166,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         const int R = r.n * p.group;
         const int n_short = ns * hkv;
         const int n_rows = (ns > 1) ? ns * R * hkv : 0;
-        const int n_long = r.qtiles * hkv;
-        int tot_s, tot_r, tot_l;
+        int tot_s, tot_r;
         const int off_s = short_base + block_exclusive_scan(n_short, tmp, &tot_s);
         const int off_r = row_base + block_exclusive_scan(n_rows, tmp, &tot_r);
-        const int off_l = long_base + block_exclusive_scan(n_long, tmp, &tot_l);
         if (r.is_short && off_s + n_short <= p.max_short && off_r + n_rows <= p.cap_rows) {
             int k = off_s;
             for (int h = 0; h < hkv; ++h) {
@@ -179,13 +188,41 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         } else if (r.is_short) {
             s_overflow = 1;
         }
-        if (r.qtiles > 0 && off_l + n_long <= p.max_long) {
-            int k = off_l;
-            // later query tiles see more keys: emit them first
-            for (int qt = r.qtiles - 1; qt >= 0; --qt) {
+        short_base += tot_s;
+        row_base += tot_r;
+    }
+
+    // 3b. tensor-core items, longest key range first (counting sort on the
+    // number of 128-key tiles), so persistent CTAs that take items in order
+    // finish together.
+    __shared__ int bins[kSortBins];
+    for (int i = tid; i < kSortBins; i += kPlanThreads) bins[i] = 0;
+    __syncthreads();
+    for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+        const ReqInfo r = load_req(p, b);
+        for (int qt = 0; qt < r.qtiles; ++qt)
+            atomicAdd(&bins[long_bin(p, r, qt)], hkv);
+    }
+    __syncthreads();
+    {
+        // one bin per thread: exclusive scan gives each bin's first slot
+        int tot_l;
+        const int v = tid < kSortBins ? bins[tid] : 0;
+        const int off = block_exclusive_scan(v, tmp, &tot_l);
+        if (tid < kSortBins) bins[tid] = off;
+        long_base = tot_l;
+        __syncthreads();
+    }
+    if (long_base > p.max_long) {
+        if (tid == 0) s_overflow = 1;
+    } else {
+        for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+            const ReqInfo r = load_req(p, b);
+            for (int qt = 0; qt < r.qtiles; ++qt) {
+                const int k0 = atomicAdd(&bins[long_bin(p, r, qt)], hkv);
                 const int nvalid = min(p.q_tile_tokens, r.n - qt * p.q_tile_tokens);
                 const int kend = min(r.len, r.ctx + qt * p.q_tile_tokens + nvalid);
-                for (int h = 0; h < hkv; ++h, ++k) {
+                for (int h = 0; h < hkv; ++h) {
                     LongItem it;
                     it.b = b;
                     it.h = h;
@@ -195,15 +232,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
                     it.key_begin = 0;
                     it.key_end = kend;
                     it.partial_base = 0;
-                    p.long_items[k] = it;
+                    p.long_items[k0 + h] = it;
                 }
             }
-        } else if (r.qtiles > 0) {
-            s_overflow = 1;
         }
-        short_base += tot_s;
-        row_base += tot_r;
-        long_base += tot_l;
     }
 
     // 4. counters and header ----------------------------------------------------
