@@ -209,6 +209,22 @@ def make_events(n):
     return pairs
 
 
+def max_over_ranks(ms: float, device) -> float:
+    """Slowest rank's time (replicas run independently; the job is as slow as
+    its slowest GPU).  A no-op without torch.distributed."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_step: int, steps: int, ms: float) -> float:
+    """Whole-job units/s: every rank processed units_per_step per step."""
+    return world * units_per_step * steps / (ms / 1000.0)
+
+
 def time_steps(fn, steps, stream):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -360,17 +376,14 @@ def run_ours(args):
     torch.cuda.synchronize()
     for w in ev:
         pk.set_profile_events(w, None, None)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     clocks = sampler.stop() if sampler else None
     status = pk.read_device_status(clear=True)
     if status:
         log(f"[bench] WARNING device status {status:#x}")
 
     ms_step = ms / args.steps
-    value = world * step.num_q_tokens * args.steps / (ms / 1000.0)
+    value = job_throughput(world, step.num_q_tokens, args.steps, ms)
     short_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[pk.PA_KERNEL_SPLIT_KV])
     long_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[pk.PA_KERNEL_TENSOR_CORE])
     achieved = short_bytes / (short_ms / 1000.0) / 1e9 if short_bytes else 0.0
@@ -420,11 +433,8 @@ def run_ours(args):
         if world > 1:
             torch.distributed.barrier()
         e_ms = time_steps(e2e_step, args.steps, stream)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * step.num_q_tokens * args.steps / (e_ms / 1000.0),
+        e_ms = max_over_ranks(e_ms, dev)
+        e2e = {"value": job_throughput(world, step.num_q_tokens, args.steps, e_ms),
                "unit": "query tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / args.steps}
 

@@ -356,7 +356,9 @@ int prefix_plan(int T, int prefix_len, int num_kv_heads, int group, int sms, int
     *q_tiles = (T + tq - 1) / tq;
     const int tiles = (prefix_len + kLongKeys - 1) / kLongKeys;
     const int pairs = num_kv_heads * *q_tiles;
-    int ns = (2 * sms + pairs - 1) / pairs;
+    // the prefix kernel is persistent (one CTA per SM): split the key range so
+    // that every (kv head, query tile, split) item gets an SM of its own
+    int ns = std::max(1, sms / std::max(1, pairs));
     ns = std::max(1, std::min(ns, std::min(64, tiles)));
     const int per = (tiles + ns - 1) / ns;  // KV tiles per split
     *split_keys = per * kLongKeys;

@@ -205,6 +205,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
         }
     }
 }
+// Warp-wide bounded wait: lane 0 polls (bounded, see mbar_wait), then every
+// lane tests the now-complete phase itself so that each thread has its own
+// acquire of the barrier, and __syncwarp keeps the compiler from moving any
+// lane's later loads or stores above the wait.  Returns the same value in
+// all lanes.
+__device__ __forceinline__ bool warp_mbar_wait(uint64_t *bar, uint32_t parity,
+                                               volatile int *abort) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) (void)mbar_try_wait(bar, parity);
+    __syncwarp();
+    return ok != 0;
+}
 // Short bounded wait used only while draining after an abort.
 __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
     const uint64_t t0 = global_timer_ns();

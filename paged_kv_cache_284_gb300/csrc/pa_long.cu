@@ -67,9 +67,7 @@ struct Bars {
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort);
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    return warp_mbar_wait(bar, parity, abort);
 }
 
 // Barrier among the 4 softmax warps built on an mbarrier with a bounded
@@ -529,7 +527,7 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                     ctl[1] = (old == it.nsplit - 1) ? 1 : 0;
                 }
                 sok = softmax_sync(&bars->sync, sync_phase, abort_flag) && sok;
-                const int last = ctl[1];
+                const int last = *reinterpret_cast<volatile int *>(&ctl[1]);
                 sok = softmax_sync(&bars->sync, sync_phase, abort_flag) && sok;  // flag read by all
                 if (sok && last && row_valid) {
                     __threadfence();

@@ -226,9 +226,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
     uint32_t it = 0;
     while (true) {
         const int slot = it % kShortStages;
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait(&full[slot], (it / kShortStages) & 1, abort_flag);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
+        const bool ok = warp_mbar_wait(&full[slot], (it / kShortStages) & 1, abort_flag);
         if (!ok) {
             if (lane == 0) flag_status(p.status, PA_DEV_WAIT_TIMEOUT);
             break;
