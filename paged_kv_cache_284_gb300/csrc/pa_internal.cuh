@@ -27,7 +27,7 @@ constexpr int kShortConsumerWarps = 4;
 constexpr int kShortThreads = 32 * (kShortConsumerWarps + 1);
 constexpr int kLongRows = 128;        // tcgen05 tile: M = 128 query rows
 constexpr int kLongKeys = 128;        // tcgen05 tile: N = 128 keys per KV tile
-constexpr int kLongThreads = 224;     // 7 warps: K+Q loads, MMA, 4 x softmax, V loads
+constexpr int kLongThreads = 352;     // 11 warps: K+Q loads, MMA, 8 x softmax, V loads
 constexpr int kPlanThreads = 1024;
 constexpr int kMinSplitStages = 4;    // 256 keys: smallest automatic split
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
@@ -330,6 +330,17 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Same MMA with the A operand (M x K, one row per TMEM lane, two 16-bit
+// elements per 32-bit column) read from tensor memory.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -379,6 +390,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
         "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+
+// One 32-bit TMEM cell per thread (lane = thread, one column).
+__device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t (&r)[1]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r[0]) : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, const uint32_t (&r)[1]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r[0])
+                 : "memory");
 }
 
 // Attention-state folding -------------------------------------------------------

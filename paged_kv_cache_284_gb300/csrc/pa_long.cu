@@ -10,17 +10,19 @@
 //  * rows of a tile are (token, head) pairs of one kv head's GQA group:
 //    128 / group tokens x group heads, loaded by one 3-D TMA box per 64 dims;
 //  * warp 0 gathers 128-key K tiles through the block table (eight 16-key TMA
-//    boxes, 128-byte swizzle) into a 3-deep ring that is released as soon as
-//    S = Q K^T has consumed it; warp 6 does the same for V into a 2-deep ring
+//    boxes, 128-byte swizzle) into a 2-deep ring that is released as soon as
+//    S = Q K^T has consumed it; warp 10 does the same for V into a 3-deep ring
 //    released after O += P V;
 //  * warp 1 issues tcgen05.mma: S = Q K^T (M=128, N=128, K=head_dim) into one
 //    of two TMEM S buffers, then O += P V (M=128, N=head_dim, K=128) into a
-//    TMEM O accumulator, V read N-major straight from its cache layout;
-//  * warps 2-5 (one thread per row) read S from TMEM, apply the
+//    TMEM O accumulator, with P read from TMEM and V read N-major straight
+//    from its cache layout;
+//  * warps 2-9 (two threads per row, one per half of its 128 keys) read S from TMEM, apply the
 //    context-offset causal mask (row i of a request with context c sees keys
 //    0..c+i), run the online softmax in the log2 domain with a lazy max
 //    update, rescale O in TMEM only when the max grows by more than 2^8, and
-//    write P (bf16) to shared memory for the next MMA;
+//    write P (bf16) into one of two TMEM P buffers; P V trails Q K^T by two
+//    tiles so the tensor cores always have the next scores to compute;
 //  * the epilogue reads O from TMEM, normalises and stores bf16 (or fp32
 //    partial states that the last split folds with the merge operator)
 //    while the next item's Q, K and V are already streaming in.
@@ -31,9 +33,10 @@ namespace pa {
 
 namespace {
 
-constexpr int kKStages = 3;
-constexpr int kVStages = 2;
-constexpr int kLongWarps = 7;  // 0: K (+Q) loads, 1: MMA, 2-5: softmax, 6: V loads
+constexpr int kKStages = 2;  // K is released as soon as Q K^T has read it
+constexpr int kVStages = 3;  // V is held until the P V two tiles later
+constexpr int kLongWarps = 11;  // 0: K (+Q) loads, 1: MMA, 2-9: softmax, 10: V loads
+constexpr int kSoftmaxWarps = 8;
 
 template <int D>
 struct LongGeom {
@@ -41,18 +44,22 @@ struct LongGeom {
     static constexpr int kHalfBytes = 128 * 128;            // 128 rows x 128 B
     static constexpr int kQBytes = kHalves * kHalfBytes;    // Q tile
     static constexpr int kKVBytes = kHalves * kHalfBytes;   // one K (or V) tile of 128 keys
-    static constexpr int kPBytes = 2 * kHalfBytes;          // P tile: 128 rows x 128 keys
     static constexpr int kOffQ = 0;
-    static constexpr int kOffP = kOffQ + kQBytes;
-    static constexpr int kOffK = kOffP + kPBytes;
+    static constexpr int kOffK = kOffQ + kQBytes;
     static constexpr int kOffV = kOffK + kKStages * kKVBytes;
     static constexpr int kOffBar = kOffV + kVStages * kKVBytes;
     static constexpr int kCtlBytes = 512;
+    // row-half exchange: partial maxima [2 tile parities][2 halves][128 rows]
+    // and partial sums [2 halves][128 rows]
+    static constexpr int kOffXchg = kOffBar + kCtlBytes;
+    static constexpr int kXchgBytes = (2 * 2 * 128 + 2 * 128) * 4;
     // at least 116 KiB so that one CTA owns an SM (and its 512 TMEM columns)
-    static constexpr int kSmemRaw = kOffBar + kCtlBytes + 1024;
+    static constexpr int kSmemRaw = kOffXchg + kXchgBytes + 1024;
     static constexpr int kSmemBytes = kSmemRaw > 116 * 1024 ? kSmemRaw : 116 * 1024;
-    static constexpr uint32_t kTmemCols = 512;  // S0 | S1 | O
-    static constexpr int kColS = 0, kColO = 2 * kLongKeys;
+    // TMEM columns: S0 | S1 (fp32 scores) | O (fp32) | P0 | P1 (bf16 pairs)
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr int kColS = 0, kColO = 2 * kLongKeys, kColP = 3 * kLongKeys;
+    static_assert(kColO + D <= kColP, "O overlaps P");
 };
 
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -63,14 +70,16 @@ struct Bars {
     uint64_t k_full[kKStages], k_empty[kKStages];
     uint64_t v_full[kVStages], v_empty[kVStages];
     uint64_t s_full[2], s_free[2];
-    uint64_t p_full, o_done, o_free, sync, drain;
+    uint64_t p_full[2];  // by tile parity: a softmax half may run a tile ahead
+    uint64_t pv_done[2];  // P V of a tile finished, by the tile's P buffer
+    uint64_t o_free, sync, xchg, drain;
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
     return warp_mbar_wait(bar, parity, abort);
 }
 
-// Barrier among the 4 softmax warps built on an mbarrier with a bounded
+// Barrier among the softmax warps built on an mbarrier with a bounded
 // wait, so a kernel that gave up elsewhere can never hang here.
 __device__ __forceinline__ bool softmax_sync(uint64_t *bar, uint32_t &phase, volatile int *abort) {
     __syncwarp();
@@ -237,12 +246,15 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->s_full[i], 1);
-            mbar_init(&bars->s_free[i], 4);
+            mbar_init(&bars->s_free[i], kSoftmaxWarps);
         }
-        mbar_init(&bars->p_full, 4);
-        mbar_init(&bars->o_done, 1);
-        mbar_init(&bars->o_free, 4);
-        mbar_init(&bars->sync, 4);
+        mbar_init(&bars->p_full[0], kSoftmaxWarps);
+        mbar_init(&bars->p_full[1], kSoftmaxWarps);
+        mbar_init(&bars->pv_done[0], 1);
+        mbar_init(&bars->pv_done[1], 1);
+        mbar_init(&bars->o_free, kSoftmaxWarps);
+        mbar_init(&bars->sync, kSoftmaxWarps);
+        mbar_init(&bars->xchg, kSoftmaxWarps);
         mbar_init(&bars->drain, 1);
         ctl[0] = 0;
         ctl[1] = 0;
@@ -257,7 +269,6 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
     uint8_t *sQ = smem + G::kOffQ;
     uint8_t *sK = smem + G::kOffK;
     uint8_t *sV = smem + G::kOffV;
-    uint8_t *sP = smem + G::kOffP;
 
     if (warp == 0) {
         // ============================ K (and Q) loads ============================
@@ -277,13 +288,12 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kLongRows, kLongKeys, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kLongRows, D, 1);
-            const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV),
-                           p_addr = smem_u32(sP);
+            const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
             uint32_t t = 0, k_item = 0;
             bool ok = true;
             // O += P V for global tile tt; `first` starts the item's accumulation
             auto issue_pv = [&](uint32_t tt, bool first) -> bool {
-                if (!mbar_wait(&bars->p_full, tt & 1, abort_flag)) return false;
+                if (!mbar_wait(&bars->p_full[tt & 1], (tt >> 1) & 1, abort_flag)) return false;
                 // the previous item's epilogue must have read O before it is reset
                 if (first && k_item > 0 &&
                     !mbar_wait(&bars->o_free, (k_item - 1) & 1, abort_flag))
@@ -292,17 +302,20 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                 if (!mbar_wait(&bars->v_full[vs], (tt / kVStages) & 1, abort_flag)) return false;
                 tc_fence_after();
                 const uint32_t vbase = v_addr + vs * G::kKVBytes;
+                // P (bf16) of this tile: row r in TMEM lane r, key k in column k / 2
+                const uint32_t pcol = tmem + G::kColP + (tt & 1) * (kLongKeys / 2);
 #pragma unroll
                 for (int kk = 0; kk < kLongKeys / 16; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(
-                        p_addr + (kk >> 2) * G::kHalfBytes + (kk & 3) * 32, 16, 1024);
                     const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, G::kHalfBytes, 1024);
-                    tc_mma(tmem + G::kColO, ad, bd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                    tc_mma_ts(tmem + G::kColO, pcol + kk * 8, bd, idesc_pv,
+                              (!first || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&bars->v_empty[vs]);
-                tc_commit(&bars->o_done);
+                tc_commit(&bars->pv_done[tt & 1]);
                 return true;
             };
+            // P V trails Q K^T by two tiles, so the scores of the next two tiles
+            // are computed while the softmax works on the current one
             for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
                 const Item it = decode_item(p, idx);
                 if (it.nt == 0) continue;
@@ -329,10 +342,13 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                     tc_commit(&bars->k_empty[ks]);
                     tc_commit(&bars->s_full[sb]);
                     if (j == it.nt - 1) tc_commit(&bars->q_empty);
-                    if (j >= 1 && !issue_pv(tt - 1, j == 1)) { ok = false; break; }
+                    if (j >= 2 && !issue_pv(tt - 2, j == 2)) { ok = false; break; }
                 }
                 if (!ok) break;
-                if (!issue_pv(t + it.nt - 1, it.nt == 1)) { ok = false; break; }
+                // the item's last (up to two) P V
+                for (int j = (it.nt > 2 ? it.nt - 2 : 0); ok && j < it.nt; ++j)
+                    ok = issue_pv(t + j, j == 0);
+                if (!ok) break;
                 t += it.nt;
                 ++k_item;
             }
@@ -344,13 +360,31 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
         }
     } else {
         // ============================ softmax + epilogue ============================
+        // Two warps per TMEM lane quarter: warps 2-5 own columns 0-63 of their
+        // rows, warps 6-9 columns 64-127.  The two halves of a row swap their
+        // partial maxima through spare TMEM columns each tile and add their
+        // partial sums once per item.
         const int wq = warp & 3;  // TMEM lane quarter of this warp
+        const int half = (warp - 2) >> 2;
         const int r = wq * 32 + lane;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const int ttok = r / p.group;
         const int jh = r - ttok * p.group;
-        uint32_t t = 0, sync_phase = 0;
+        const int c0 = half * (kLongKeys / 2);  // first S / P column of this half
+        const int o0 = half * (D / 2);          // first O column of this half
+        uint32_t t = 0, sync_phase = 0, x_phase = 0;
         bool ok = true;
+        // swap one float with the other half of the row (same row, other warp)
+        float *xch = reinterpret_cast<float *>(smem + G::kOffXchg);
+        auto swap_halves = [&](float *slots, float mine, float &theirs) -> bool {
+            slots[half * 128 + r] = mine;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->xchg);
+            const bool w = warp_wait(&bars->xchg, x_phase & 1, abort_flag);
+            ++x_phase;
+            theirs = slots[(1 - half) * 128 + r];
+            return w;
+        };
         for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
             const Item it = decode_item(p, idx);
             const bool row_valid = ttok < it.nvalid && r < p.q_tile_tokens * p.group;
@@ -362,12 +396,10 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                 const int sb = tt & 1;
                 if (!warp_wait(&bars->s_full[sb], (tt >> 1) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t s0[32], s1[32], s2[32], s3[32];
-                const uint32_t sa = t_lane + G::kColS + sb * kLongKeys;
+                uint32_t s0[32], s1[32];
+                const uint32_t sa = t_lane + G::kColS + sb * kLongKeys + c0;
                 tmem_ld32(sa, s0);
                 tmem_ld32(sa + 32, s1);
-                tmem_ld32(sa + 64, s2);
-                tmem_ld32(sa + 96, s3);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
@@ -376,22 +408,26 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                 const bool need_mask =
                     (kb + kLongKeys - 1 > tile_limit_min) || (kb + kLongKeys > it.key_end);
                 if (need_mask) {
-                    // keys [0, lim) of this tile are visible to this row
-                    const int lim = min(row_limit, it.key_end - 1) - kb + 1;
+                    // keys [0, lim) of this half are visible to this row
+                    const int lim = min(row_limit, it.key_end - 1) - (kb + c0) + 1;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         if (i >= lim) s0[i] = __float_as_uint(-INFINITY);
                         if (32 + i >= lim) s1[i] = __float_as_uint(-INFINITY);
-                        if (64 + i >= lim) s2[i] = __float_as_uint(-INFINITY);
-                        if (96 + i >= lim) s3[i] = __float_as_uint(-INFINITY);
                     }
                 }
-                float mx = -INFINITY;
+                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(s0[i]), __uint_as_float(s1[i])),
-                                         fmaxf(__uint_as_float(s2[i]), __uint_as_float(s3[i]))));
+                for (int i = 0; i < 16; ++i) {
+                    mx0 = fmaxf(mx0, __uint_as_float(s0[i]));
+                    mx1 = fmaxf(mx1, __uint_as_float(s0[16 + i]));
+                    mx2 = fmaxf(mx2, __uint_as_float(s1[i]));
+                    mx3 = fmaxf(mx3, __uint_as_float(s1[16 + i]));
                 }
+                float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+                float other;
+                if (!swap_halves(xch + (tt & 1) * 256, mx, other)) { ok = false; break; }
+                mx = fmaxf(mx, other);
                 const float mxs = mx * p.scale_log2;  // scale > 0: max commutes with it
                 float alpha = 1.f;
                 if (mxs > m_used + kRescaleThreshold || (m_used == -INFINITY && mxs > -INFINITY)) {
@@ -399,40 +435,36 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                     m_used = mxs;
                 }
                 const float neg_ref = m_used == -INFINITY ? 0.f : -m_used;
-                float sum = 0.f;
-                uint32_t pk[64];
+                float sum0 = 0.f, sum1 = 0.f;
+                uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const float a0 = fast_exp2(fmaf(__uint_as_float(s0[2 * i]), p.scale_log2, neg_ref));
                     const float a1 = fast_exp2(fmaf(__uint_as_float(s0[2 * i + 1]), p.scale_log2, neg_ref));
                     const float b0 = fast_exp2(fmaf(__uint_as_float(s1[2 * i]), p.scale_log2, neg_ref));
                     const float b1 = fast_exp2(fmaf(__uint_as_float(s1[2 * i + 1]), p.scale_log2, neg_ref));
-                    const float c0 = fast_exp2(fmaf(__uint_as_float(s2[2 * i]), p.scale_log2, neg_ref));
-                    const float c1 = fast_exp2(fmaf(__uint_as_float(s2[2 * i + 1]), p.scale_log2, neg_ref));
-                    const float d0 = fast_exp2(fmaf(__uint_as_float(s3[2 * i]), p.scale_log2, neg_ref));
-                    const float d1 = fast_exp2(fmaf(__uint_as_float(s3[2 * i + 1]), p.scale_log2, neg_ref));
-                    sum += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+                    sum0 += a0 + a1;
+                    sum1 += b0 + b1;
                     pk[i] = pack_bf16x2(a0, a1);
                     pk[16 + i] = pack_bf16x2(b0, b1);
-                    pk[32 + i] = pack_bf16x2(c0, c1);
-                    pk[48 + i] = pack_bf16x2(d0, d1);
                 }
-                l = l * alpha + sum;
-                // the P buffer and the O accumulator: the previous tile's P V must be done
-                if (tt >= 1) {
-                    if (!warp_wait(&bars->o_done, (tt - 1) & 1, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                }
+                l = l * alpha + (sum0 + sum1);
                 if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    // O is rescaled in place: the previous tile's P V must be done
+                    if (!warp_wait(&bars->pv_done[(tt - 1) & 1], ((tt - 1) >> 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     uint32_t raw[32];
 #pragma unroll
-                    for (int qd = 0; qd < D / 32; ++qd) {
-                        tmem_ld32(t_lane + G::kColO + qd * 32, raw);
+                    for (int qd = 0; qd < D / 64; ++qd) {
+                        tmem_ld32(t_lane + G::kColO + o0 + qd * 32, raw);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             raw[i] = __float_as_uint(__uint_as_float(raw[i]) * alpha);
-                        tmem_st32(t_lane + G::kColO + qd * 32, raw);
+                        tmem_st32(t_lane + G::kColO + o0 + qd * 32, raw);
                     }
                     tmem_wait_st();
                 }
@@ -444,7 +476,7 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                     const int z0 = it.key_end - kb;                  // first row to clear
                     const int z1 = min(kLongKeys, (z0 + 15) & ~15);  // end of its chunk
                     const int pieces = (z1 - z0) * 8 * G::kHalves;   // 16-byte pieces
-                    for (int q = r; q < pieces; q += 128) {
+                    for (int q = r + half * 128; q < pieces; q += 256) {
                         const int hf = q / ((z1 - z0) * 8);
                         const int rem = q - hf * (z1 - z0) * 8;
                         const int row = z0 + rem / 8, piece = rem % 8;
@@ -452,23 +484,33 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                                                    row * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
                     }
                 }
-                // P row r (bf16) into the K-major, 128-byte swizzled A-operand tile
-#pragma unroll
-                for (int c16 = 0; c16 < kLongKeys / 8; ++c16) {
-                    const uint4 v = make_uint4(pk[c16 * 4 + 0], pk[c16 * 4 + 1], pk[c16 * 4 + 2],
-                                               pk[c16 * 4 + 3]);
-                    *reinterpret_cast<uint4 *>(sP + (c16 >> 3) * G::kHalfBytes +
-                                               sw128_offset(r, c16 & 7)) = v;
+                // this half's 64 keys of P row r (bf16 pairs) into the tile's TMEM
+                // P buffer, the A operand of its P V; the P V that used this buffer
+                // two tiles ago must be done
+                if (tt >= 2 && !warp_wait(&bars->pv_done[sb], ((tt - 2) >> 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-                fence_proxy_async_smem();
+                tc_fence_after();
+                tmem_st32(t_lane + G::kColP + sb * (kLongKeys / 2) + half * 32, pk);
+                tmem_wait_st();
+                if (kb + kLongKeys > it.key_end) fence_proxy_async_smem();  // zeroed V rows
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->p_full);
+                if (lane == 0) mbar_arrive(&bars->p_full[sb]);
             }
-            if (ok && it.nt > 0) ok = warp_wait(&bars->o_done, (t + it.nt - 1) & 1, abort_flag);
+            if (ok && it.nt > 0) {
+                const uint32_t last = t + it.nt - 1;
+                ok = warp_wait(&bars->pv_done[last & 1], (last >> 1) & 1, abort_flag);
+            }
             tc_fence_after();
+            if (ok && it.nt > 0) {
+                float l_other = 0.f;
+                ok = swap_halves(xch + 512, l, l_other);
+                l += l_other;
+            }
 
-            // ---- epilogue of this item ----
+            // ---- epilogue of this item: this half's D/2 output columns ----
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const float lse_v = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
             const int tok = it.tok0 + ttok;
@@ -476,10 +518,11 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
             const int64_t orow = static_cast<int64_t>(tok) * p.num_q_heads + hq;
             const bool direct = it.nsplit == 1;
             const int64_t prow = static_cast<int64_t>(it.partial_base + it.split * kLongRows + r);
-            for (int qd = 0; qd < D / 32; ++qd) {
+            for (int qd = 0; qd < D / 64; ++qd) {
+                const int col = o0 + qd * 32;
                 uint32_t raw[32];
                 if (ok && it.nt > 0) {
-                    tmem_ld32(t_lane + G::kColO + qd * 32, raw);
+                    tmem_ld32(t_lane + G::kColO + col, raw);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
@@ -487,7 +530,7 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                 }
                 if (!ok || !row_valid) continue;
                 if (direct && !p.out_f32) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + qd * 32);
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + col);
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4) {
                         uint4 w;
@@ -498,7 +541,7 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                         dst[v4] = w;
                     }
                 } else {
-                    float *dst = direct ? p.out_f32 + orow * D + qd * 32 : p.partial_o + prow * D + qd * 32;
+                    float *dst = direct ? p.out_f32 + orow * D + col : p.partial_o + prow * D + col;
 #pragma unroll
                     for (int v4 = 0; v4 < 8; ++v4)
                         __stcg(reinterpret_cast<float4 *>(dst) + v4,
@@ -510,7 +553,7 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
             tc_fence_before();
             __syncwarp();
             if (it.nt > 0 && lane == 0) mbar_arrive(&bars->o_free);
-            if (ok && row_valid) {
+            if (ok && row_valid && half == 0) {
                 if (direct) {
                     if (p.lse) p.lse[orow] = lse_v;
                 } else {
@@ -519,10 +562,11 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
             }
             if (!direct) {
                 // fused split epilogue: the last split of this (kv head, query
-                // tile) folds the partial states with the merge operator
+                // tile) folds the partial states with the merge operator; each
+                // half of a row folds its own D/2 columns
                 __threadfence();
                 bool sok = softmax_sync(&bars->sync, sync_phase, abort_flag);
-                if (sok && r == 0) {
+                if (sok && r == 0 && half == 0) {
                     const int old = atomicAdd(p.counters + it.counter_idx, 1);
                     ctl[1] = (old == it.nsplit - 1) ? 1 : 0;
                 }
@@ -544,7 +588,7 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                         wsum += w[s2];
                     }
                     const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
-                    for (int e4 = 0; e4 < D / 4; ++e4) {
+                    for (int e4 = o0 / 4; e4 < (o0 + D / 2) / 4; ++e4) {
                         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                         for (int s2 = 0; s2 < ns; ++s2) {
                             const float4 v = __ldcg(reinterpret_cast<const float4 *>(
@@ -567,7 +611,7 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                             reinterpret_cast<uint2 *>(p.out + orow * D)[e4] = pk2;
                         }
                     }
-                    if (p.lse) p.lse[orow] = wsum > 0.f ? M + __logf(wsum) : -INFINITY;
+                    if (p.lse && half == 0) p.lse[orow] = wsum > 0.f ? M + __logf(wsum) : -INFINITY;
                 }
             }
             t += it.nt;
