@@ -27,7 +27,7 @@ constexpr int kShortConsumerWarps = 4;
 constexpr int kShortThreads = 32 * (kShortConsumerWarps + 1);
 constexpr int kLongRows = 128;        // tcgen05 tile: M = 128 query rows
 constexpr int kLongKeys = 128;        // tcgen05 tile: N = 128 keys per KV tile
-constexpr int kLongThreads = 352;     // 11 warps: K+Q loads, MMA, 8 x softmax, V loads
+constexpr int kLongThreads = 384;     // 12 warps: K+Q loads, QK^T, 8 x softmax, V loads, PV
 constexpr int kPlanThreads = 1024;
 constexpr int kMinSplitStages = 4;    // 256 keys: smallest automatic split
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
@@ -392,6 +392,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
 // One 32-bit TMEM cell per thread (lane = thread, one column).
 __device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t (&r)[1]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r[0]) : "r"(taddr));

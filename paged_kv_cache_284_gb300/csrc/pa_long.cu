@@ -13,8 +13,9 @@
 //    boxes, 128-byte swizzle) into a 2-deep ring that is released as soon as
 //    S = Q K^T has consumed it; warp 10 does the same for V into a 3-deep ring
 //    released after O += P V;
-//  * warp 1 issues tcgen05.mma: S = Q K^T (M=128, N=128, K=head_dim) into one
-//    of two TMEM S buffers, then O += P V (M=128, N=head_dim, K=128) into a
+//  * warp 1 issues tcgen05.mma S = Q K^T (M=128, N=128, K=head_dim) into one
+//    of two TMEM S buffers as soon as K and a buffer are free; warp 11 issues
+//    O += P V (M=128, N=head_dim, K=128) as soon as P is ready, into a
 //    TMEM O accumulator, with P read from TMEM and V read N-major straight
 //    from its cache layout;
 //  * warps 2-9 (two threads per row, one per half of its 128 keys) read S from TMEM, apply the
@@ -35,7 +36,10 @@ namespace {
 
 constexpr int kKStages = 2;  // K is released as soon as Q K^T has read it
 constexpr int kVStages = 3;  // V is held until the P V two tiles later
-constexpr int kLongWarps = 11;  // 0: K (+Q) loads, 1: MMA, 2-9: softmax, 10: V loads
+// warps: 0 K (+Q) loads, 1 Q K^T issuer (+TMEM allocation), 2-9 softmax, 10 V loads,
+// 11 P V issuer
+constexpr int kLongWarps = 12;
+constexpr int kWarpV = 10, kWarpPV = 11;
 constexpr int kSoftmaxWarps = 8;
 
 template <int D>
@@ -72,7 +76,7 @@ struct Bars {
     uint64_t s_full[2], s_free[2];
     uint64_t p_full[2];  // by tile parity: a softmax half may run a tile ahead
     uint64_t pv_done[2];  // P V of a tile finished, by the tile's P buffer
-    uint64_t o_free, sync, xchg, drain;
+    uint64_t o_free, sync, xchg, drain, drain_pv;
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
@@ -256,6 +260,7 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
         mbar_init(&bars->sync, kSoftmaxWarps);
         mbar_init(&bars->xchg, kSoftmaxWarps);
         mbar_init(&bars->drain, 1);
+        mbar_init(&bars->drain_pv, 1);
         ctl[0] = 0;
         ctl[1] = 0;
         fence_mbar_init();
@@ -278,44 +283,20 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
         }
         produce<D, kKStages>(p, &tmk, sK, bars->k_full, bars->k_empty, bars, true, &tmq, sQ,
                              abort_flag);
-    } else if (warp == kLongWarps - 1) {
+    } else if (warp == kWarpV) {
         // ============================ V loads ============================
         if (lane == 0) tma_prefetch_desc(&tmv);
         produce<D, kVStages>(p, &tmv, sV, bars->v_full, bars->v_empty, bars, false, nullptr,
                              nullptr, abort_flag);
     } else if (warp == 1) {
-        // ============================ MMA issuer ============================
+        // ============================ Q K^T issuer ============================
+        // Runs ahead of the softmax: a tile's scores only wait for its K tile and
+        // for the softmax to have read the scores two tiles back.
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kLongRows, kLongKeys, 0);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(kLongRows, D, 1);
-            const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+            const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK);
             uint32_t t = 0, k_item = 0;
             bool ok = true;
-            // O += P V for global tile tt; `first` starts the item's accumulation
-            auto issue_pv = [&](uint32_t tt, bool first) -> bool {
-                if (!mbar_wait(&bars->p_full[tt & 1], (tt >> 1) & 1, abort_flag)) return false;
-                // the previous item's epilogue must have read O before it is reset
-                if (first && k_item > 0 &&
-                    !mbar_wait(&bars->o_free, (k_item - 1) & 1, abort_flag))
-                    return false;
-                const int vs = tt % kVStages;
-                if (!mbar_wait(&bars->v_full[vs], (tt / kVStages) & 1, abort_flag)) return false;
-                tc_fence_after();
-                const uint32_t vbase = v_addr + vs * G::kKVBytes;
-                // P (bf16) of this tile: row r in TMEM lane r, key k in column k / 2
-                const uint32_t pcol = tmem + G::kColP + (tt & 1) * (kLongKeys / 2);
-#pragma unroll
-                for (int kk = 0; kk < kLongKeys / 16; ++kk) {
-                    const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, G::kHalfBytes, 1024);
-                    tc_mma_ts(tmem + G::kColO, pcol + kk * 8, bd, idesc_pv,
-                              (!first || kk > 0) ? 1u : 0u);
-                }
-                tc_commit(&bars->v_empty[vs]);
-                tc_commit(&bars->pv_done[tt & 1]);
-                return true;
-            };
-            // P V trails Q K^T by two tiles, so the scores of the next two tiles
-            // are computed while the softmax works on the current one
             for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
                 const Item it = decode_item(p, idx);
                 if (it.nt == 0) continue;
@@ -342,13 +323,7 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                     tc_commit(&bars->k_empty[ks]);
                     tc_commit(&bars->s_full[sb]);
                     if (j == it.nt - 1) tc_commit(&bars->q_empty);
-                    if (j >= 2 && !issue_pv(tt - 2, j == 2)) { ok = false; break; }
                 }
-                if (!ok) break;
-                // the item's last (up to two) P V
-                for (int j = (it.nt > 2 ? it.nt - 2 : 0); ok && j < it.nt; ++j)
-                    ok = issue_pv(t + j, j == 0);
-                if (!ok) break;
                 t += it.nt;
                 ++k_item;
             }
@@ -356,6 +331,49 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                 // let every MMA already issued finish before TMEM is released
                 tc_commit(&bars->drain);
                 mbar_drain(&bars->drain, 0);
+            }
+        }
+    } else if (warp == kWarpPV) {
+        // ============================ P V issuer ============================
+        // Follows the softmax: a tile's P V waits for its P, its V tile and, at
+        // the start of an item, for the previous item's epilogue to read O.
+        if (lane == 0) {
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(kLongRows, D, 1);
+            const uint32_t v_addr = smem_u32(sV);
+            uint32_t t = 0, k_item = 0;
+            bool ok = true;
+            for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+                const Item it = decode_item(p, idx);
+                if (it.nt == 0) continue;
+                for (int j = 0; j < it.nt; ++j) {
+                    const uint32_t tt = t + j;
+                    if (!mbar_wait(&bars->p_full[tt & 1], (tt >> 1) & 1, abort_flag)) { ok = false; break; }
+                    if (j == 0 && k_item > 0 &&
+                        !mbar_wait(&bars->o_free, (k_item - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const int vs = tt % kVStages;
+                    if (!mbar_wait(&bars->v_full[vs], (tt / kVStages) & 1, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t vbase = v_addr + vs * G::kKVBytes;
+                    // P (bf16) of this tile: row r in TMEM lane r, key k in column k / 2
+                    const uint32_t pcol = tmem + G::kColP + (tt & 1) * (kLongKeys / 2);
+#pragma unroll
+                    for (int kk = 0; kk < kLongKeys / 16; ++kk) {
+                        const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, G::kHalfBytes, 1024);
+                        tc_mma_ts(tmem + G::kColO, pcol + kk * 8, bd, idesc_pv,
+                                  (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&bars->v_empty[vs]);
+                    tc_commit(&bars->pv_done[tt & 1]);
+                }
+                t += it.nt;
+                ++k_item;
+            }
+            if (!ok) {
+                tc_commit(&bars->drain_pv);
+                mbar_drain(&bars->drain_pv, 0);
             }
         }
     } else {
