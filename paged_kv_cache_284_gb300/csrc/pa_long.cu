@@ -76,7 +76,8 @@ struct Bars {
     uint64_t s_full[2], s_free[2];
     uint64_t p_full[2];  // by tile parity: a softmax half may run a tile ahead
     uint64_t pv_done[2];  // P V of a tile finished, by the tile's P buffer
-    uint64_t o_free, sync, xchg, drain, drain_pv;
+    uint64_t xchg[4];  // row-half exchange, one per TMEM lane quarter (2 warps each)
+    uint64_t o_free, sync, drain, drain_pv;
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
         mbar_init(&bars->pv_done[1], 1);
         mbar_init(&bars->o_free, kSoftmaxWarps);
         mbar_init(&bars->sync, kSoftmaxWarps);
-        mbar_init(&bars->xchg, kSoftmaxWarps);
+        for (int i = 0; i < 4; ++i) mbar_init(&bars->xchg[i], 2);
         mbar_init(&bars->drain, 1);
         mbar_init(&bars->drain_pv, 1);
         ctl[0] = 0;
@@ -397,8 +398,8 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
         auto swap_halves = [&](float *slots, float mine, float &theirs) -> bool {
             slots[half * 128 + r] = mine;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->xchg);
-            const bool w = warp_wait(&bars->xchg, x_phase & 1, abort_flag);
+            if (lane == 0) mbar_arrive(&bars->xchg[wq]);
+            const bool w = warp_wait(&bars->xchg[wq], x_phase & 1, abort_flag);
             ++x_phase;
             theirs = slots[(1 - half) * 128 + r];
             return w;
@@ -453,20 +454,48 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                     m_used = mxs;
                 }
                 const float neg_ref = m_used == -INFINITY ? 0.f : -m_used;
-                float sum0 = 0.f, sum1 = 0.f;
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float a0 = fast_exp2(fmaf(__uint_as_float(s0[2 * i]), p.scale_log2, neg_ref));
-                    const float a1 = fast_exp2(fmaf(__uint_as_float(s0[2 * i + 1]), p.scale_log2, neg_ref));
-                    const float b0 = fast_exp2(fmaf(__uint_as_float(s1[2 * i]), p.scale_log2, neg_ref));
-                    const float b1 = fast_exp2(fmaf(__uint_as_float(s1[2 * i + 1]), p.scale_log2, neg_ref));
-                    sum0 += a0 + a1;
-                    sum1 += b0 + b1;
-                    pk[i] = pack_bf16x2(a0, a1);
-                    pk[16 + i] = pack_bf16x2(b0, b1);
+                // this half's 64 keys of P row r (bf16 pairs) go to the tile's TMEM
+                // P buffer, the A operand of its P V, in two 32-key pieces so the
+                // first store overlaps the second piece's exponentials; the P V
+                // that used this buffer two tiles ago must be done
+                if (tt >= 2 && !warp_wait(&bars->pv_done[sb], ((tt - 2) >> 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-                l = l * alpha + (sum0 + sum1);
+                tc_fence_after();
+                const uint32_t pdst = t_lane + G::kColP + sb * (kLongKeys / 2) + half * 32;
+                float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+                {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2) {
+                        const float a0 = fast_exp2(fmaf(__uint_as_float(s0[2 * i]), p.scale_log2, neg_ref));
+                        const float a1 = fast_exp2(fmaf(__uint_as_float(s0[2 * i + 1]), p.scale_log2, neg_ref));
+                        const float a2 = fast_exp2(fmaf(__uint_as_float(s0[2 * i + 2]), p.scale_log2, neg_ref));
+                        const float a3 = fast_exp2(fmaf(__uint_as_float(s0[2 * i + 3]), p.scale_log2, neg_ref));
+                        sum0 += a0 + a1;
+                        sum1 += a2 + a3;
+                        pk[i] = pack_bf16x2(a0, a1);
+                        pk[i + 1] = pack_bf16x2(a2, a3);
+                    }
+                    tmem_st16(pdst, pk);
+                }
+                {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2) {
+                        const float b0 = fast_exp2(fmaf(__uint_as_float(s1[2 * i]), p.scale_log2, neg_ref));
+                        const float b1 = fast_exp2(fmaf(__uint_as_float(s1[2 * i + 1]), p.scale_log2, neg_ref));
+                        const float b2 = fast_exp2(fmaf(__uint_as_float(s1[2 * i + 2]), p.scale_log2, neg_ref));
+                        const float b3 = fast_exp2(fmaf(__uint_as_float(s1[2 * i + 3]), p.scale_log2, neg_ref));
+                        sum2 += b0 + b1;
+                        sum3 += b2 + b3;
+                        pk[i] = pack_bf16x2(b0, b1);
+                        pk[i + 1] = pack_bf16x2(b2, b3);
+                    }
+                    tmem_st16(pdst + 16, pk);
+                }
+                l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
                 if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
                     // O is rescaled in place: the previous tile's P V must be done
                     if (!warp_wait(&bars->pv_done[(tt - 1) & 1], ((tt - 1) >> 1) & 1, abort_flag)) {
@@ -502,15 +531,6 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                                                    row * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
                     }
                 }
-                // this half's 64 keys of P row r (bf16 pairs) into the tile's TMEM
-                // P buffer, the A operand of its P V; the P V that used this buffer
-                // two tiles ago must be done
-                if (tt >= 2 && !warp_wait(&bars->pv_done[sb], ((tt - 2) >> 1) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                tmem_st32(t_lane + G::kColP + sb * (kLongKeys / 2) + half * 32, pk);
                 tmem_wait_st();
                 if (kb + kLongKeys > it.key_end) fence_proxy_async_smem();  // zeroed V rows
                 tc_fence_before();
