@@ -139,6 +139,14 @@ __device__ __forceinline__ Item decode_item(const LongParams &p, int idx) {
     return it;
 }
 
+// Item a CTA takes in round k: items are sorted longest first, and the CTAs
+// take them in serpentine order (left to right, then right to left), which
+// keeps the per-CTA totals close to a longest-processing-time schedule.
+__device__ __forceinline__ int serpentine_item(int round) {
+    const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    return round * g + ((round & 1) ? g - 1 - c : c);
+}
+
 __device__ __forceinline__ int num_items(const LongParams &p) {
     if (p.prefix_mode) return p.num_kv_heads * p.prefix_q_tiles * p.prefix_nsplit;
     return *reinterpret_cast<volatile int *>(&p.hdr->num_long_items);
@@ -156,7 +164,9 @@ __device__ void produce(const LongParams &p, const CUtensorMap *tm, uint8_t *rin
     uint32_t t = 0;        // tiles issued by this warp so far (all items)
     uint32_t k_item = 0;   // items (with keys) started so far
     bool ok = true;
-    for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+    for (int round = 0; ok && round * static_cast<int>(gridDim.x) < n_items; ++round) {
+        const int idx = serpentine_item(round);
+        if (idx >= n_items) continue;
         const Item it = decode_item(p, idx);
         if (it.nt == 0) continue;
         if (load_q) {
@@ -298,7 +308,9 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
             const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK);
             uint32_t t = 0, k_item = 0;
             bool ok = true;
-            for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+            for (int round = 0; ok && round * static_cast<int>(gridDim.x) < n_items; ++round) {
+        const int idx = serpentine_item(round);
+        if (idx >= n_items) continue;
                 const Item it = decode_item(p, idx);
                 if (it.nt == 0) continue;
                 if (!mbar_wait(&bars->q_full, k_item & 1, abort_flag)) { ok = false; break; }
@@ -343,7 +355,9 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
             const uint32_t v_addr = smem_u32(sV);
             uint32_t t = 0, k_item = 0;
             bool ok = true;
-            for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+            for (int round = 0; ok && round * static_cast<int>(gridDim.x) < n_items; ++round) {
+        const int idx = serpentine_item(round);
+        if (idx >= n_items) continue;
                 const Item it = decode_item(p, idx);
                 if (it.nt == 0) continue;
                 for (int j = 0; j < it.nt; ++j) {
@@ -404,7 +418,9 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
             theirs = slots[(1 - half) * 128 + r];
             return w;
         };
-        for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+        for (int round = 0; ok && round * static_cast<int>(gridDim.x) < n_items; ++round) {
+        const int idx = serpentine_item(round);
+        if (idx >= n_items) continue;
             const Item it = decode_item(p, idx);
             const bool row_valid = ttok < it.nvalid && r < p.q_tile_tokens * p.group;
             const int row_limit = it.causal ? it.pos0 + ttok : 0x7fffffff;
