@@ -77,6 +77,27 @@ struct Consumer {
     float m0, m1, l0, l1;
 };
 
+// Block id of chunk first_stage*4 + lane of a split-KV item (one lane per
+// chunk of an 8-stage batch), or -1 past the item's keys.  Out-of-range
+// table columns and block ids are clamped and flagged.
+__device__ __forceinline__ int block_id_of(const ShortParams &p, const ShortItem &item, int L,
+                                           int first_stage, int lane) {
+    const int key_end = min(item.stage_end * kStageKeys, L);
+    const int key0 = (first_stage * kStageChunks + lane) * kChunkKeys;
+    if (key0 >= key_end) return -1;
+    int col = key0 / p.block_size;
+    if (col >= p.bt_stride) {  // seq_len beyond the table row
+        flag_status(p.status, PA_DEV_BAD_METADATA);
+        col = p.bt_stride - 1;
+    }
+    int blk = __ldg(p.block_tables + static_cast<int64_t>(item.b) * p.bt_stride + col);
+    if (blk < 0 || blk >= p.num_blocks) {
+        flag_status(p.status, PA_DEV_BAD_BLOCK);
+        blk = min(max(blk, 0), p.num_blocks - 1);
+    }
+    return blk;
+}
+
 }  // namespace
 
 template <int D>
@@ -125,11 +146,22 @@ __global__ void __launch_bounds__(kShortThreads, 2)
         }
         uint32_t it = 0;
         bool aborted = false;
+        // The next item's index, descriptor, length and first block ids are
+        // fetched one step per stage while the current item is still being
+        // issued, and block ids are read one 8-stage batch ahead, so the ring
+        // never waits on a chain of dependent global loads.
+        int cur_idx = 0;
+        if (lane == 0) cur_idx = atomicAdd(&p.hdr->short_next, 1);
+        cur_idx = __shfl_sync(0xffffffffu, cur_idx, 0);
+        ShortItem cur{};
+        int cur_L = 0, cur_blk = -1;
+        if (cur_idx < num_items) {
+            cur = p.items[cur_idx];
+            cur_L = __ldg(p.seq_lens + cur.b);
+            cur_blk = block_id_of(p, cur, cur_L, cur.stage_begin, lane);
+        }
         while (!aborted) {
-            int item_idx = 0;
-            if (lane == 0) item_idx = atomicAdd(&p.hdr->short_next, 1);
-            item_idx = __shfl_sync(0xffffffffu, item_idx, 0);
-            if (item_idx >= num_items) {
+            if (cur_idx >= num_items) {
                 const int slot = it % kShortStages;
                 bool ok = true;
                 if (lane == 0) {
@@ -143,35 +175,22 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                 __syncwarp();
                 break;
             }
-            const ShortItem item = p.items[item_idx];
-            const int L = __ldg(p.seq_lens + item.b);
-            const int key_end = min(item.stage_end * kStageKeys, L);
-            const int *bt = p.block_tables + static_cast<int64_t>(item.b) * p.bt_stride;
-            int my_blk = -1;
-            for (int st = item.stage_begin; st < item.stage_end; ++st, ++it) {
-                const int rel = st - item.stage_begin;
+            int nxt_idx = 0;
+            if (lane == 0) nxt_idx = atomicAdd(&p.hdr->short_next, 1);  // read two stages later
+            ShortItem nxt{};
+            int nxt_L = 0, nxt_blk = -1, pf = 0;  // prefetch state of the next item
+            const int nst = cur.stage_end - cur.stage_begin;
+            int batch_blk = cur_blk, next_batch = -1;
+            for (int rel = 0; rel < nst; ++rel, ++it) {
+                const int st = cur.stage_begin + rel;
                 if ((rel & 7) == 0) {
-                    // block ids of the next 32 chunks (8 stages), one per lane
-                    const int key0 = (st * kStageChunks + lane) * kChunkKeys;
-                    my_blk = -1;
-                    if (key0 < key_end) {
-                        int col = key0 / p.block_size;
-                        if (col >= p.bt_stride) {  // seq_len beyond the table row
-                            flag_status(p.status, PA_DEV_BAD_METADATA);
-                            col = p.bt_stride - 1;
-                        }
-                        int blk = __ldg(bt + col);
-                        if (blk < 0 || blk >= p.num_blocks) {
-                            flag_status(p.status, PA_DEV_BAD_BLOCK);
-                            blk = min(max(blk, 0), p.num_blocks - 1);
-                        }
-                        my_blk = blk;
-                    }
+                    if (rel > 0) batch_blk = next_batch;
+                    next_batch = (rel + 8 < nst) ? block_id_of(p, cur, cur_L, st + 8, lane) : -1;
                 }
                 int blks[kStageChunks];
 #pragma unroll
                 for (int c = 0; c < kStageChunks; ++c)
-                    blks[c] = __shfl_sync(0xffffffffu, my_blk, (rel & 7) * kStageChunks + c);
+                    blks[c] = __shfl_sync(0xffffffffu, batch_blk, (rel & 7) * kStageChunks + c);
                 const int slot = it % kShortStages;
                 int ok = 1;
                 if (lane == 0 && it >= kShortStages)
@@ -186,10 +205,9 @@ __global__ void __launch_bounds__(kShortThreads, 2)
 #pragma unroll
                     for (int c = 0; c < kStageChunks; ++c) nvalid += blks[c] >= 0;
                     StageMeta mm;
-                    mm.item = item_idx;
+                    mm.item = cur_idx;
                     mm.stage = st;
-                    mm.flags = (st == item.stage_begin ? kFirst : 0) |
-                               (st == item.stage_end - 1 ? kLast : 0);
+                    mm.flags = (rel == 0 ? kFirst : 0) | (rel == nst - 1 ? kLast : 0);
                     mm.pad = 0;
                     meta[slot] = mm;
                     mbar_arrive_expect_tx(&full[slot],
@@ -198,7 +216,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                     for (int c = 0; c < kStageChunks; ++c) {
                         if (blks[c] < 0) continue;
                         const int key0 = (st * kStageChunks + c) * kChunkKeys;
-                        const int row = (blks[c] * p.num_kv_heads + item.h) * p.block_size +
+                        const int row = (blks[c] * p.num_kv_heads + cur.h) * p.block_size +
                                         key0 % p.block_size;
 #pragma unroll
                         for (int hf = 0; hf < G::kHalves; ++hf) {
@@ -208,7 +226,31 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                     }
                 }
                 __syncwarp();
+                // one prefetch step per stage from the third stage on; the last
+                // stage finishes whatever is left
+                for (;;) {
+                    if (pf == 0 && (rel >= 2 || rel == nst - 1)) {
+                        nxt_idx = __shfl_sync(0xffffffffu, nxt_idx, 0);
+                        if (nxt_idx < num_items) nxt = p.items[nxt_idx];
+                        pf = 1;
+                    } else if (pf == 1 && (rel >= 3 || rel == nst - 1)) {
+                        if (nxt_idx < num_items) nxt_L = __ldg(p.seq_lens + nxt.b);
+                        pf = 2;
+                    } else if (pf == 2 && (rel >= 4 || rel == nst - 1)) {
+                        if (nxt_idx < num_items)
+                            nxt_blk = block_id_of(p, nxt, nxt_L, nxt.stage_begin, lane);
+                        pf = 3;
+                    } else {
+                        break;
+                    }
+                    if (rel != nst - 1) break;
+                }
             }
+            if (aborted) break;
+            cur_idx = nxt_idx;
+            cur = nxt;
+            cur_L = nxt_L;
+            cur_blk = nxt_blk;
         }
         if (aborted && lane == 0) {
             flag_status(p.status, PA_DEV_WAIT_TIMEOUT);
@@ -498,42 +540,58 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                 }
             }
             if (cs.nsplit > 1) {
-                // fused split-KV epilogue: the last split of (b, h) folds all partials
-                __threadfence();
+                // fused split-KV epilogue: the last split of (b, h) folds all
+                // partials.  One thread releases this CTA's partial writes
+                // (ordered before it by the CTA barrier) with a GPU-scope fence
+                // and the counter update, and acquires the others' if last.
                 named_bar_sync(1, 32 * kShortConsumerWarps);
                 if (threadIdx.x == 0) {
+                    __threadfence();
                     const int old = atomicAdd(p.counters + cs.b * p.num_kv_heads + cs.h, 1);
-                    ctl[1] = (old == cs.nsplit - 1) ? 1 : 0;
+                    const int last = (old == cs.nsplit - 1) ? 1 : 0;
+                    if (last) __threadfence();
+                    ctl[1] = last;
                 }
                 named_bar_sync(1, 32 * kShortConsumerWarps);
-                if (ctl[1]) {
-                    __threadfence();
+                if (*reinterpret_cast<volatile int *>(&ctl[1])) {
                     const int base = cs.partial_base - cs.split * cs.R;
-                    const int total = cs.R * D;
-                    for (int idx = threadIdx.x; idx < total; idx += 32 * kShortConsumerWarps) {
-                        const int r = idx / D, e = idx - r * D;
+                    const int total4 = cs.R * (D / 4);
+                    for (int idx = threadIdx.x; idx < total4; idx += 32 * kShortConsumerWarps) {
+                        const int r = idx / (D / 4), e4 = idx - r * (D / 4);
                         const int tok = cs.tok0 + r / p.group;
                         const int hq = cs.h * p.group + r % p.group;
                         const int64_t row = static_cast<int64_t>(tok) * p.num_q_heads + hq;
                         const float xl = p.extra_o ? __ldg(p.extra_lse + row) : -INFINITY;
                         const float M = lse_max_of(p.partial_lse + base + r, cs.R, cs.nsplit, xl);
-                        float acc = 0.f, wsum = 0.f;
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                        float wsum = 0.f;
                         if (M != -INFINITY) {
-                            for (int s = 0; s < cs.nsplit; ++s) {
-                                const float ls = __ldcg(p.partial_lse + base + s * cs.R + r);
-                                const float w = __expf(ls - M);
+                            for (int s2 = 0; s2 < cs.nsplit; ++s2) {
+                                const float w = __expf(__ldcg(p.partial_lse + base + s2 * cs.R + r) - M);
+                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(
+                                    p.partial_o + static_cast<int64_t>(base + s2 * cs.R + r) * D) + e4);
                                 wsum += w;
-                                acc += w * __ldcg(p.partial_o + static_cast<int64_t>(base + s * cs.R + r) * D + e);
+                                acc.x += w * v.x;
+                                acc.y += w * v.y;
+                                acc.z += w * v.z;
+                                acc.w += w * v.w;
                             }
                             if (p.extra_o) {
                                 const float w = __expf(xl - M);
+                                const float4 v = __ldg(reinterpret_cast<const float4 *>(p.extra_o + row * D) + e4);
                                 wsum += w;
-                                acc += w * __ldg(p.extra_o + row * D + e);
+                                acc.x += w * v.x;
+                                acc.y += w * v.y;
+                                acc.z += w * v.z;
+                                acc.w += w * v.w;
                             }
                         }
-                        const float val = wsum > 0.f ? acc / wsum : 0.f;
-                        p.out[row * D + e] = __float2bfloat16_rn(val);
-                        if (e == 0 && p.lse) p.lse[row] = wsum > 0.f ? M + __logf(wsum) : -INFINITY;
+                        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+                        uint2 pk2;
+                        pk2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+                        pk2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+                        reinterpret_cast<uint2 *>(p.out + row * D)[e4] = pk2;
+                        if (e4 == 0 && p.lse) p.lse[row] = wsum > 0.f ? M + __logf(wsum) : -INFINITY;
                     }
                 }
                 named_bar_sync(1, 32 * kShortConsumerWarps);
