@@ -245,7 +245,7 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
     pp.short_max_rows = forbid_long ? 0x7fffffff : short_max_rows;
     pp.split_stages = split_keys / kStageKeys;
     const int short_grid = dev->sms * dev->short_ctas_per_sm[D == 128 ? 1 : 0];
-    pp.target_items = 12 * short_grid;
+    pp.target_items = kSplitItemsPerCta * short_grid;
     pp.hdr = hdr;
     pp.short_items = reinterpret_cast<ShortItem *>(ws + L.short_items);
     pp.long_items = reinterpret_cast<LongItem *>(ws + L.long_items);
@@ -319,6 +319,9 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
         lp.partial_o = sp.partial_o;
         lp.partial_lse = sp.partial_lse;
         lp.status = dev->status;
+        // the split-KV kernel was launched just before: the tensor-core grid
+        // may take over SMs as split-KV CTAs finish (its rows are disjoint)
+        lp.overlap_prev = short_grid > 0 ? 1 : 0;
         // a long request has q_len * group > short_max_rows, so there are at
         // most T / (short_max_rows / group + 1) of them
         const int min_long_tokens = short_max_rows / group + 1;

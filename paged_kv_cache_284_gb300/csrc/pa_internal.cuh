@@ -30,12 +30,17 @@ constexpr int kLongKeys = 128;        // tcgen05 tile: N = 128 keys per KV tile
 constexpr int kLongThreads = 384;     // 12 warps: K+Q loads, QK^T, 8 x softmax, V loads, PV
 constexpr int kPlanThreads = 1024;
 constexpr int kMinSplitStages = 4;    // 256 keys: smallest automatic split
+// Automatic split size: total split-KV stages / (this x persistent CTAs).  The
+// items are taken longest first, so a request is cut only when it is long
+// next to a CTA's share of the step (each split costs a partial-state write
+// and a fold).
+constexpr int kSplitItemsPerCta = 3;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
 
 // Work list written by the plan kernel into the caller's workspace.
 struct PlanHeader {
-    int num_short_items;
-    int num_long_items;
+    int num_short_items;   // work items (records x Hkv)
+    int num_long_items;    // work items (records x Hkv)
     int short_next;        // dynamic work counter of the split-KV kernel
     int long_next;         // dynamic work counter of the tensor-core kernel
     int split_stages;      // chosen split size (in 64-key stages)
@@ -44,24 +49,47 @@ struct PlanHeader {
 };
 static_assert(sizeof(PlanHeader) == 64, "header size");
 
-// One split-KV work item: kv head h of request b, keys
-// [stage_begin*64, min(stage_end*64, seq_len)).
-struct ShortItem {
-    int b, h, split, nsplit;
-    int stage_begin, stage_end;
-    int partial_base;  // first partial row of this split (nsplit > 1)
-    int pad;
+// Work records written by the plan kernel.  A record covers every kv head:
+// work item i of a kernel is record i / Hkv for kv head i % Hkv, so the plan
+// writes one 32-byte record (two 16-byte stores) per request split or query
+// tile instead of one per kv head.
+
+// Split-KV record: request b, keys [stage_begin*64, min(stage_end*64, seq_len)).
+// Split s of kv head h writes partial rows partial_base + h*nsplit*R + [0, R)
+// (R = q_len * group) when nsplit > 1.
+struct alignas(16) ShortItem {
+    int b, split, nsplit, stage_begin;
+    int stage_end, partial_base, pad0, pad1;
 };
 static_assert(sizeof(ShortItem) == 32, "item size");
 
-// One tensor-core work item: kv head h of request b, query tile q_tile
-// (tile = 128/group tokens x group heads), keys [key_begin, key_end).
-struct LongItem {
-    int b, h, q_tile, split, nsplit;
-    int key_begin, key_end;
-    int partial_base;
+// Tensor-core record: query tile q_tile of request b (tile = 128/group tokens
+// x group heads), keys [key_begin, key_end).
+struct alignas(16) LongItem {
+    int b, q_tile, key_begin, key_end;
+    int pad[4];
 };
 static_assert(sizeof(LongItem) == 32, "item size");
+
+#if defined(__CUDACC__)
+// Records are read through L2 (the plan kernel that wrote them may have run
+// concurrently with this grid's launch).
+template <typename T>
+__device__ __forceinline__ T load_record(const T *base, int rec) {
+    static_assert(sizeof(T) == 32, "record size");
+    T r;
+    const int4 *src = reinterpret_cast<const int4 *>(base + rec);
+    *reinterpret_cast<int4 *>(&r) = __ldcg(src);
+    *(reinterpret_cast<int4 *>(&r) + 1) = __ldcg(src + 1);
+    return r;
+}
+template <typename T>
+__device__ __forceinline__ void store_record(T *base, int rec, const T &r) {
+    int4 *dst = reinterpret_cast<int4 *>(base + rec);
+    dst[0] = *reinterpret_cast<const int4 *>(&r);
+    dst[1] = *(reinterpret_cast<const int4 *>(&r) + 1);
+}
+#endif
 
 // Byte offsets of the workspace regions (same computation on host and device).
 struct WsLayout {
@@ -105,6 +133,11 @@ struct LongParams {
     int *counters;
     float *partial_o, *partial_lse;
     unsigned *status;
+    // 1: launched as a programmatic dependent of the split-KV kernel of the
+    // same step.  The kernel then reads nothing but the plan's output (and
+    // the step's inputs) before its last instruction, where it waits for the
+    // split-KV grid so that its own completion still orders the stream.
+    int overlap_prev;
 };
 
 struct PlanParams {
@@ -119,6 +152,27 @@ struct PlanParams {
     int *counters;
     int max_short, max_long, cap_rows, num_counters;
     unsigned *status;
+};
+
+// Launch configuration with the programmatic-stream-serialisation attribute
+// (programmatic dependent launch): the kernel may be scheduled while the
+// previous kernel of the stream is still running, and must call pdl_wait()
+// before it touches anything that kernel (or an earlier one) produces.
+struct PdlLaunch {
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    PdlLaunch(dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl = true) {
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+    }
+    PdlLaunch(const PdlLaunch &) = delete;
+    PdlLaunch &operator=(const PdlLaunch &) = delete;
 };
 
 // Host-side launchers (each defined next to its kernel).
@@ -168,6 +222,14 @@ __device__ __forceinline__ void flag_status(unsigned *status, unsigned bits) {
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
 }
+// Programmatic dependent launch: wait until the previous grid of the stream
+// has completed and its memory is visible (a no-op for a plain launch), and
+// allow the next grid to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -408,16 +470,6 @@ __device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t (&r)[1]) {
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, const uint32_t (&r)[1]) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r[0])
                  : "memory");
-}
-
-// Attention-state folding -------------------------------------------------------
-// A state is (o normalised, lse natural log).  Fold partial states of one
-// (row, element): returns the merged o element and, via *lse_out, the merged
-// lse.  Empty states carry lse = -inf and contribute nothing.
-__device__ __forceinline__ float lse_max_of(const float *lse, int stride, int n, float extra) {
-    float m = extra;
-    for (int s = 0; s < n; ++s) m = fmaxf(m, __ldcg(lse + static_cast<size_t>(s) * stride));
-    return m;
 }
 
 #endif  // __CUDACC__

@@ -110,9 +110,10 @@ __device__ __forceinline__ Item decode_item(const LongParams &p, int idx) {
     Item it{};
     const int TQ = p.q_tile_tokens;
     if (!p.prefix_mode) {
-        const LongItem li = p.items[idx];
+        const int rec = idx / p.num_kv_heads;
+        const LongItem li = load_record(p.items, rec);
         it.b = li.b;
-        it.h = li.h;
+        it.h = idx - rec * p.num_kv_heads;
         const int q0 = __ldg(p.qsl + li.b);
         const int n = __ldg(p.qsl + li.b + 1) - q0;
         it.tok0 = q0 + li.q_tile * TQ;
@@ -245,7 +246,10 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_items = num_items(p);
-    if (static_cast<int>(blockIdx.x) >= n_items) return;
+    if (static_cast<int>(blockIdx.x) >= n_items) {
+        pdl_wait();  // complete only after the grid this one overlaps
+        return;
+    }
 
     // ---- setup ----------------------------------------------------------------
     if (threadIdx.x == 0) {
@@ -677,6 +681,9 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, G::kTmemCols);
+    // with overlap_prev: this grid completes only after the split-KV grid it
+    // overlapped, so later work on the stream is still ordered after both
+    pdl_wait();
 }
 
 size_t long_smem_bytes(int head_dim) {
@@ -705,14 +712,18 @@ int launch_long(const LongParams &p, const CUtensorMap &tq, const CUtensorMap &t
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return PA_ERR_CUDA;
     grid = grid < sms ? grid : sms;
+    const bool pdl = p.overlap_prev != 0;
     if (head_dim == 128) {
         if (configure_long<128>() != PA_OK) return PA_ERR_CUDA;
-        long_kernel<128><<<grid, 32 * kLongWarps, LongGeom<128>::kSmemBytes, s>>>(p, tq, tk, tv);
-    } else {
-        if (configure_long<64>() != PA_OK) return PA_ERR_CUDA;
-        long_kernel<64><<<grid, 32 * kLongWarps, LongGeom<64>::kSmemBytes, s>>>(p, tq, tk, tv);
+        PdlLaunch l(grid, 32 * kLongWarps, LongGeom<128>::kSmemBytes, s, pdl);
+        return cudaLaunchKernelEx(&l.cfg, long_kernel<128>, p, tq, tk, tv) == cudaSuccess
+                   ? PA_OK
+                   : PA_ERR_CUDA;
     }
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    if (configure_long<64>() != PA_OK) return PA_ERR_CUDA;
+    PdlLaunch l(grid, 32 * kLongWarps, LongGeom<64>::kSmemBytes, s, pdl);
+    return cudaLaunchKernelEx(&l.cfg, long_kernel<64>, p, tq, tk, tv) == cudaSuccess ? PA_OK
+                                                                                    : PA_ERR_CUDA;
 }
 
 }  // namespace pa

@@ -102,32 +102,50 @@ __device__ __forceinline__ int long_bin(const PlanParams &p, const ReqInfo &r, i
     return kSortBins - 1 - min(tiles, kSortBins - 1);
 }
 
+// Sort bin of a split-KV item of `stages` stages: bin 0 holds the longest.
+__device__ __forceinline__ int short_bin(int stages) {
+    return kSortBins - 1 - min(stages, kSortBins - 1);
+}
+
+// First stage of split s of ns over `stages` stages (s = ns gives the end).
+__device__ __forceinline__ int split_begin(int stages, int ns, int s) {
+    return static_cast<int>(static_cast<long long>(stages) * s / ns);
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     __shared__ int tmp[33];
     __shared__ long long tmpl[33];
-    __shared__ int s_split;
-    __shared__ int s_overflow;
-    const int tid = threadIdx.x;
-    if (tid == 0) s_overflow = 0;
+    __shared__ int bins[kSortBins];
+    __shared__ int s_split, s_overflow, s_max_stages;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int hkv = p.num_kv_heads;
+    // the metadata (and the workspace) may belong to the previous kernel
+    pdl_wait();
+    pdl_trigger();
+    if (tid == 0) {
+        s_overflow = 0;
+        s_max_stages = 0;
+    }
+    for (int i = tid; i < kSortBins; i += kPlanThreads) bins[i] = 0;
+    // Request tid's metadata is read once and kept in registers; only steps
+    // with more than kPlanThreads requests read the others again per pass.
+    const ReqInfo mine = tid < p.num_seqs ? load_req(p, tid) : ReqInfo{};
+    auto req = [&](int b) { return b == tid ? mine : load_req(p, b); };
+    __syncthreads();
 
     // 1. total split-KV work (in stages) -------------------------------------
-    long long work = 0, max_stages = 0;
+    long long work = 0;
+    int max_stages = 0;
     for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
-        const ReqInfo r = load_req(p, b);
+        const ReqInfo r = req(b);
         if (r.is_short) {
             work += r.stages;
-            max_stages = max(max_stages, static_cast<long long>(r.stages));
+            max_stages = max(max_stages, r.stages);
         }
     }
-    const long long total_work = block_sum_ll(work, tmpl) * hkv;
-    // block max via the same reduction on negated values is awkward; use a
-    // shared atomic instead.
-    __shared__ int s_max_stages;
-    if (tid == 0) s_max_stages = 0;
-    __syncthreads();
-    atomicMax(&s_max_stages, static_cast<int>(max_stages));
-    __syncthreads();
+    max_stages = __reduce_max_sync(0xffffffffu, max_stages);
+    if (lane == 0 && max_stages > 0) atomicMax(&s_max_stages, max_stages);
+    const long long total_work = block_sum_ll(work, tmpl) * hkv;  // also orders the atomics
 
     // 2. split size ------------------------------------------------------------
     int sp;
@@ -141,7 +159,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     for (int guard = 0; guard < 40; ++guard) {
         long long items = 0, rows = 0;
         for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
-            const ReqInfo r = load_req(p, b);
+            const ReqInfo r = req(b);
             if (!r.is_short) continue;
             const int ns = (r.stages + sp - 1) / sp;
             items += ns;
@@ -156,52 +174,68 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     __syncthreads();
     sp = s_split;
 
-    // 3. emit items, request by request in rounds of kPlanThreads -------------
     int short_base = 0, long_base = 0, row_base = 0;
+
+    // 3. split-KV items, longest key range first (counting sort on the number
+    // of stages of the item).  A request's ns splits cut its stages into
+    // ranges that differ by at most one stage.  Partial-state rows are
+    // handed out in request order by a block scan.
+    for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+        const ReqInfo r = req(b);
+        if (!r.is_short) continue;
+        const int ns = (r.stages + sp - 1) / sp;
+        for (int s = 0; s < ns; ++s)
+            atomicAdd(&bins[short_bin(split_begin(r.stages, ns, s + 1) -
+                                      split_begin(r.stages, ns, s))],
+                      1);
+    }
+    __syncthreads();
+    {
+        int tot_s;
+        const int v = tid < kSortBins ? bins[tid] : 0;
+        const int off = block_exclusive_scan(v, tmp, &tot_s);
+        if (tid < kSortBins) bins[tid] = off;
+        short_base = tot_s;  // records
+        __syncthreads();
+    }
     for (int b0 = 0; b0 < p.num_seqs; b0 += kPlanThreads) {
         const int b = b0 + tid;
         ReqInfo r{};
-        if (b < p.num_seqs) r = load_req(p, b);
+        if (b < p.num_seqs) r = req(b);
         const int ns = r.is_short ? (r.stages + sp - 1) / sp : 0;
         const int R = r.n * p.group;
-        const int n_short = ns * hkv;
         const int n_rows = (ns > 1) ? ns * R * hkv : 0;
-        int tot_s, tot_r;
-        const int off_s = short_base + block_exclusive_scan(n_short, tmp, &tot_s);
+        int tot_r;
         const int off_r = row_base + block_exclusive_scan(n_rows, tmp, &tot_r);
-        if (r.is_short && off_s + n_short <= p.max_short && off_r + n_rows <= p.cap_rows) {
-            int k = off_s;
-            for (int h = 0; h < hkv; ++h) {
-                for (int s = 0; s < ns; ++s, ++k) {
-                    ShortItem it;
-                    it.b = b;
-                    it.h = h;
-                    it.split = s;
-                    it.nsplit = ns;
-                    it.stage_begin = s * sp;
-                    it.stage_end = min((s + 1) * sp, r.stages);
-                    it.partial_base = (ns > 1) ? off_r + (h * ns + s) * R : 0;
-                    it.pad = 0;
-                    p.short_items[k] = it;
-                }
-            }
-        } else if (r.is_short) {
-            s_overflow = 1;
-        }
-        short_base += tot_s;
         row_base += tot_r;
+        if (static_cast<long long>(short_base) * hkv > p.max_short || row_base > p.cap_rows) {
+            if (tid == 0) s_overflow = 1;
+            continue;  // uniform: both totals are block-wide
+        }
+        for (int s = 0; s < ns; ++s) {
+            const int s0 = split_begin(r.stages, ns, s), s1 = split_begin(r.stages, ns, s + 1);
+            ShortItem it;
+            it.b = b;
+            it.split = s;
+            it.nsplit = ns;
+            it.stage_begin = s0;
+            it.stage_end = s1;
+            it.partial_base = (ns > 1) ? off_r + s * R : 0;
+            it.pad0 = it.pad1 = 0;
+            store_record(p.short_items, atomicAdd(&bins[short_bin(s1 - s0)], 1), it);
+        }
     }
+    __syncthreads();
 
     // 3b. tensor-core items, longest key range first (counting sort on the
     // number of 128-key tiles), so persistent CTAs that take items in order
     // finish together.
-    __shared__ int bins[kSortBins];
     for (int i = tid; i < kSortBins; i += kPlanThreads) bins[i] = 0;
     __syncthreads();
     for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
-        const ReqInfo r = load_req(p, b);
+        const ReqInfo r = req(b);
         for (int qt = 0; qt < r.qtiles; ++qt)
-            atomicAdd(&bins[long_bin(p, r, qt)], hkv);
+            atomicAdd(&bins[long_bin(p, r, qt)], 1);
     }
     __syncthreads();
     {
@@ -213,27 +247,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         long_base = tot_l;
         __syncthreads();
     }
-    if (long_base > p.max_long) {
+    if (static_cast<long long>(long_base) * hkv > p.max_long) {
         if (tid == 0) s_overflow = 1;
     } else {
         for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
-            const ReqInfo r = load_req(p, b);
+            const ReqInfo r = req(b);
             for (int qt = 0; qt < r.qtiles; ++qt) {
-                const int k0 = atomicAdd(&bins[long_bin(p, r, qt)], hkv);
                 const int nvalid = min(p.q_tile_tokens, r.n - qt * p.q_tile_tokens);
-                const int kend = min(r.len, r.ctx + qt * p.q_tile_tokens + nvalid);
-                for (int h = 0; h < hkv; ++h) {
-                    LongItem it;
-                    it.b = b;
-                    it.h = h;
-                    it.q_tile = qt;
-                    it.split = 0;
-                    it.nsplit = 1;
-                    it.key_begin = 0;
-                    it.key_end = kend;
-                    it.partial_base = 0;
-                    p.long_items[k0 + h] = it;
-                }
+                LongItem it{};
+                it.b = b;
+                it.q_tile = qt;
+                it.key_begin = 0;
+                it.key_end = min(r.len, r.ctx + qt * p.q_tile_tokens + nvalid);
+                store_record(p.long_items, atomicAdd(&bins[long_bin(p, r, qt)], 1), it);
             }
         }
     }
@@ -244,8 +270,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     if (tid == 0) {
         // A work list that did not fit is never run partially: no items at all.
         if (s_overflow) flag_status(p.status, PA_DEV_PLAN_OVERFLOW);
-        p.hdr->num_short_items = s_overflow ? 0 : short_base;
-        p.hdr->num_long_items = s_overflow ? 0 : long_base;
+        p.hdr->num_short_items = s_overflow ? 0 : short_base * hkv;
+        p.hdr->num_long_items = s_overflow ? 0 : long_base * hkv;
         p.hdr->short_next = 0;
         p.hdr->long_next = 0;
         p.hdr->split_stages = sp;
@@ -254,8 +280,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
 }
 
 int launch_plan(const PlanParams &p, cudaStream_t s) {
-    plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    PdlLaunch l(1, kPlanThreads, 0, s);
+    return cudaLaunchKernelEx(&l.cfg, plan_kernel, p) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace pa

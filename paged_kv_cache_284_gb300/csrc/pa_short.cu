@@ -46,6 +46,7 @@ struct StageMeta {
 constexpr int kFirst = 1, kLast = 2;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: lazy max update
+constexpr int kFoldBatch = 8;              // splits loaded together by the fold
 
 __device__ __forceinline__ float quad_max(float v) {
     v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
@@ -98,6 +99,13 @@ __device__ __forceinline__ int block_id_of(const ShortParams &p, const ShortItem
     return blk;
 }
 
+// Work item idx: its record and kv head.
+__device__ __forceinline__ ShortItem short_work(const ShortParams &p, int idx, int &h) {
+    const int rec = idx / p.num_kv_heads;
+    h = idx - rec * p.num_kv_heads;
+    return load_record(p.items, rec);
+}
+
 }  // namespace
 
 template <int D>
@@ -126,7 +134,14 @@ __global__ void __launch_bounds__(kShortThreads, 2)
         ctl[1] = 0;
         fence_mbar_init();
     }
+    if (warp == kShortConsumerWarps && lane == 0) {
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+    }
     __syncthreads();
+    // everything below reads the plan's output
+    pdl_wait();
+    pdl_trigger();
 
     auto k_box = [&](int slot, int c, int hf) -> uint8_t * {
         return stage_mem + slot * G::kStageBytes + (c * G::kHalves + hf) * G::kBoxBytes;
@@ -140,10 +155,6 @@ __global__ void __launch_bounds__(kShortThreads, 2)
 
     if (warp == kShortConsumerWarps) {
         // ============================ producer ============================
-        if (lane == 0) {
-            tma_prefetch_desc(&tmk);
-            tma_prefetch_desc(&tmv);
-        }
         uint32_t it = 0;
         bool aborted = false;
         // The next item's index, descriptor, length and first block ids are
@@ -154,9 +165,9 @@ __global__ void __launch_bounds__(kShortThreads, 2)
         if (lane == 0) cur_idx = atomicAdd(&p.hdr->short_next, 1);
         cur_idx = __shfl_sync(0xffffffffu, cur_idx, 0);
         ShortItem cur{};
-        int cur_L = 0, cur_blk = -1;
+        int cur_h = 0, cur_L = 0, cur_blk = -1;
         if (cur_idx < num_items) {
-            cur = p.items[cur_idx];
+            cur = short_work(p, cur_idx, cur_h);
             cur_L = __ldg(p.seq_lens + cur.b);
             cur_blk = block_id_of(p, cur, cur_L, cur.stage_begin, lane);
         }
@@ -178,7 +189,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
             int nxt_idx = 0;
             if (lane == 0) nxt_idx = atomicAdd(&p.hdr->short_next, 1);  // read two stages later
             ShortItem nxt{};
-            int nxt_L = 0, nxt_blk = -1, pf = 0;  // prefetch state of the next item
+            int nxt_h = 0, nxt_L = 0, nxt_blk = -1, pf = 0;  // prefetch state of the next item
             const int nst = cur.stage_end - cur.stage_begin;
             int batch_blk = cur_blk, next_batch = -1;
             for (int rel = 0; rel < nst; ++rel, ++it) {
@@ -216,7 +227,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                     for (int c = 0; c < kStageChunks; ++c) {
                         if (blks[c] < 0) continue;
                         const int key0 = (st * kStageChunks + c) * kChunkKeys;
-                        const int row = (blks[c] * p.num_kv_heads + cur.h) * p.block_size +
+                        const int row = (blks[c] * p.num_kv_heads + cur_h) * p.block_size +
                                         key0 % p.block_size;
 #pragma unroll
                         for (int hf = 0; hf < G::kHalves; ++hf) {
@@ -231,7 +242,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                 for (;;) {
                     if (pf == 0 && (rel >= 2 || rel == nst - 1)) {
                         nxt_idx = __shfl_sync(0xffffffffu, nxt_idx, 0);
-                        if (nxt_idx < num_items) nxt = p.items[nxt_idx];
+                        if (nxt_idx < num_items) nxt = short_work(p, nxt_idx, nxt_h);
                         pf = 1;
                     } else if (pf == 1 && (rel >= 3 || rel == nst - 1)) {
                         if (nxt_idx < num_items) nxt_L = __ldg(p.seq_lens + nxt.b);
@@ -249,6 +260,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
             if (aborted) break;
             cur_idx = nxt_idx;
             cur = nxt;
+            cur_h = nxt_h;
             cur_L = nxt_L;
             cur_blk = nxt_blk;
         }
@@ -278,18 +290,19 @@ __global__ void __launch_bounds__(kShortThreads, 2)
 
         if (mm.flags & kFirst) {
             // ---- item setup ----
-            const ShortItem item = p.items[mm.item];
+            int item_h;
+            const ShortItem item = short_work(p, mm.item, item_h);
             cs.b = item.b;
-            cs.h = item.h;
+            cs.h = item_h;
             cs.split = item.split;
             cs.nsplit = item.nsplit;
-            cs.partial_base = item.partial_base;
             cs.tok0 = __ldg(p.qsl + item.b);
             const int n = __ldg(p.qsl + item.b + 1) - cs.tok0;
             cs.ctx = __ldg(p.ctx + item.b);
             const int L = __ldg(p.seq_lens + item.b);
             cs.key_end = min(item.stage_end * kStageKeys, L);
             cs.R = n * p.group;
+            cs.partial_base = item.partial_base + item_h * item.nsplit * cs.R;
             const int RT = (cs.R + 15) >> 4;
             const int RTp = RT >= 3 ? 4 : RT;
             cs.KQ = kShortConsumerWarps / RTp;
@@ -562,19 +575,40 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                         const int hq = cs.h * p.group + r % p.group;
                         const int64_t row = static_cast<int64_t>(tok) * p.num_q_heads + hq;
                         const float xl = p.extra_o ? __ldg(p.extra_lse + row) : -INFINITY;
-                        const float M = lse_max_of(p.partial_lse + base + r, cs.R, cs.nsplit, xl);
+                        const float *pl = p.partial_lse + base + r;
+                        const float4 *po = reinterpret_cast<const float4 *>(
+                                               p.partial_o + static_cast<int64_t>(base + r) * D) + e4;
+                        const int64_t ostride = static_cast<int64_t>(cs.R) * (D / 4);
+                        // splits are read kFoldBatch at a time so their L2
+                        // round trips overlap
+                        float M = xl;
+                        for (int s0 = 0; s0 < cs.nsplit; s0 += kFoldBatch) {
+#pragma unroll
+                            for (int j = 0; j < kFoldBatch; ++j)
+                                if (s0 + j < cs.nsplit) M = fmaxf(M, __ldcg(pl + (s0 + j) * cs.R));
+                        }
                         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                         float wsum = 0.f;
                         if (M != -INFINITY) {
-                            for (int s2 = 0; s2 < cs.nsplit; ++s2) {
-                                const float w = __expf(__ldcg(p.partial_lse + base + s2 * cs.R + r) - M);
-                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-                                    p.partial_o + static_cast<int64_t>(base + s2 * cs.R + r) * D) + e4);
-                                wsum += w;
-                                acc.x += w * v.x;
-                                acc.y += w * v.y;
-                                acc.z += w * v.z;
-                                acc.w += w * v.w;
+                            for (int s0 = 0; s0 < cs.nsplit; s0 += kFoldBatch) {
+                                float lv[kFoldBatch];
+                                float4 v[kFoldBatch];
+#pragma unroll
+                                for (int j = 0; j < kFoldBatch; ++j) {
+                                    const bool in = s0 + j < cs.nsplit;
+                                    lv[j] = in ? __ldcg(pl + (s0 + j) * cs.R) : -INFINITY;
+                                    v[j] = in ? __ldcg(po + (s0 + j) * ostride)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                                }
+#pragma unroll
+                                for (int j = 0; j < kFoldBatch; ++j) {
+                                    const float w = __expf(lv[j] - M);
+                                    wsum += w;
+                                    acc.x += w * v[j].x;
+                                    acc.y += w * v[j].y;
+                                    acc.z += w * v[j].z;
+                                    acc.w += w * v[j].w;
+                                }
                             }
                             if (p.extra_o) {
                                 const float w = __expf(xl - M);
@@ -639,12 +673,14 @@ int launch_short(const ShortParams &p, const CUtensorMap &tk, const CUtensorMap 
     if (grid <= 0) return PA_OK;
     if (head_dim == 128) {
         if (configure_short<128>() != PA_OK) return PA_ERR_CUDA;
-        short_kernel<128><<<grid, kShortThreads, ShortGeom<128>::kSmemBytes, s>>>(p, tk, tv);
-    } else {
-        if (configure_short<64>() != PA_OK) return PA_ERR_CUDA;
-        short_kernel<64><<<grid, kShortThreads, ShortGeom<64>::kSmemBytes, s>>>(p, tk, tv);
+        PdlLaunch l(grid, kShortThreads, ShortGeom<128>::kSmemBytes, s);
+        return cudaLaunchKernelEx(&l.cfg, short_kernel<128>, p, tk, tv) == cudaSuccess ? PA_OK
+                                                                                      : PA_ERR_CUDA;
     }
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    if (configure_short<64>() != PA_OK) return PA_ERR_CUDA;
+    PdlLaunch l(grid, kShortThreads, ShortGeom<64>::kSmemBytes, s);
+    return cudaLaunchKernelEx(&l.cfg, short_kernel<64>, p, tk, tv) == cudaSuccess ? PA_OK
+                                                                                 : PA_ERR_CUDA;
 }
 
 }  // namespace pa

@@ -13,6 +13,10 @@ __global__ void __launch_bounds__(256) write_kv_kernel(
     const uint4 *__restrict__ k, const uint4 *__restrict__ v, const int64_t *__restrict__ slots,
     int num_tokens, int num_kv_heads, int pieces_per_row, int block_size, int num_blocks,
     uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, unsigned *status) {
+    // k, v and the slots may come from the previous kernel, and that kernel
+    // may still read the cache
+    pdl_wait();
+    pdl_trigger();
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t per_token = static_cast<int64_t>(num_kv_heads) * pieces_per_row;
     if (idx >= per_token * num_tokens) return;
@@ -42,11 +46,12 @@ int launch_write_kv(const void *k, const void *v, const int64_t *slots, int num_
     const int64_t total = static_cast<int64_t>(num_tokens) * kv->num_kv_heads * pieces;
     const int threads = 256;
     const int64_t blocks = (total + threads - 1) / threads;
-    write_kv_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slots, num_tokens,
-        kv->num_kv_heads, pieces, kv->block_size, kv->num_blocks,
+    PdlLaunch l(static_cast<unsigned>(blocks), threads, 0, s);
+    const cudaError_t e = cudaLaunchKernelEx(
+        &l.cfg, write_kv_kernel, static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slots,
+        num_tokens, kv->num_kv_heads, pieces, kv->block_size, kv->num_blocks,
         static_cast<uint4 *>(kv->k_cache), static_cast<uint4 *>(kv->v_cache), status);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace pa
