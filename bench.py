@@ -456,12 +456,13 @@ def run_ours(args):
     gpu_launches = 4 * args.steps   # write_kv, plan, split-KV, tensor-core per step
 
     # ---- secondary: decode-heavy KV GB/s and cascade --------------------------
-    decode = cascade = None
+    decode = cascade = graph = None
     del ds
     torch.cuda.empty_cache()
     if not args.no_secondary:
         decode = bench_decode_heavy(args, dev, hbm_peak)
         cascade = bench_cascade(args, dev)
+        graph = bench_graph_decode(args, dev)
 
     # ---- CPU baseline (rank 0 only) -----------------------------------------
     cpu = None
@@ -493,6 +494,7 @@ def run_ours(args):
             "kernels": {"split_kv": split_kv, "tensor_core": tensor_core},
             "decode_heavy": decode,
             "cascade": cascade,
+            "graph_decode": graph,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clocks,
@@ -537,6 +539,41 @@ def bench_decode_heavy(args, dev, hbm_peak):
            "split_kv_kernel_gbs": alg / (k_ms / 1000) / 1e9,
            "split_kv_kernel_frac": alg / (k_ms / 1000) / 1e9 / hbm_peak}
     del ds
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_graph_decode(args, dev):
+    """Small decode steps (write + attention) launched one by one versus
+    replayed from one captured CUDA graph: the launch overhead the on-device
+    plan lets a serving loop remove."""
+    from paged_kv_cache_284_gb300 import workloads
+    res = {"workload": "decode rows, seq_len U[512,4096], 32 q / 8 kv heads, d=128, bs=16; "
+                       "write_kv + attention per step, back to back"}
+    for b in (8, 64):
+        pool, (step,) = workloads.decode_heavy(seed=workloads.SEED_BASE + 50 + b, num_seqs=b)
+        ds = DeviceStep(pool, step, dev)
+        stream = torch.cuda.current_stream()
+        for _ in range(max(3, args.warmup)):
+            ds.run()
+        torch.cuda.synchronize()
+        n = max(args.steps, 50)
+        eager = time_steps(ds.run, n, stream) / n
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            ds.run()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            ds.run()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        graph = time_steps(g.replay, n, stream) / n
+        res[f"batch_{b}"] = {"eager_ms": eager, "graph_ms": graph, "speedup": eager / graph}
+        del g, ds
     torch.cuda.empty_cache()
     return res
 

@@ -283,6 +283,35 @@ def cascade(seed: int = SEED_BASE + 4, num_seqs: int = 64, prefix_len: int = 819
     return pool, [step]
 
 
+def graph_replay_pair(seed: int = SEED_BASE + 5, num_decode: int = 12, num_spec: int = 2,
+                      spec_len: int = 5, chunk_len: int = 40, ctx: Tuple[int, int] = (16, 1500),
+                      num_q_heads: int = 8, num_kv_heads: int = 2, head_dim: int = 128,
+                      block_size: int = 16):
+    """Two steps with identical shapes on one pool -- the same request count,
+    q_lens (decode rows, speculative-verify rows, one chunk long enough for
+    the tensor-core path) and block-table width -- but their own context
+    lengths, blocks and values: one step is captured in a CUDA graph, the
+    other is replayed through it."""
+    gen = torch.Generator().manual_seed(seed)
+
+    def draw():
+        dec = _uniform_int(ctx[0], ctx[1], num_decode, gen)
+        spec = _uniform_int(ctx[0], ctx[1], num_spec, gen)
+        chunk = _uniform_int(0, ctx[1], 1, gen)
+        return ([(L - 1, 1) for L in dec] + [(c, spec_len) for c in spec]
+                + [(c, chunk_len) for c in chunk])
+
+    ra, rb = draw(), draw()
+    nb, tables, _ = _assign_tables(ra + rb, block_size, gen)
+    pool = make_pool(nb, num_kv_heads, block_size, head_dim, gen)
+    mb = max(len(t) for t in tables)
+    kw = dict(num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+              block_size=block_size, gen=gen, max_blocks=mb)
+    sa = build_step(ra, tables=tables[:len(ra)], label="graph_capture", **kw)
+    sb = build_step(rb, tables=tables[len(ra):], label="graph_replay", **kw)
+    return pool, [sa, sb]
+
+
 CONFIGS = {
     "tiny_prefill": tiny_prefill,
     "chunked_prefix_decode": chunked_prefix_decode,
