@@ -20,9 +20,14 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 def attention(q_bits, kc_bits, vc_bits, block_tables, qsl, ctx, seq_lens, scale):
-    q = bf16_bits_to_f64(np.asarray(q_bits))
-    kc = bf16_bits_to_f64(np.asarray(kc_bits))
-    vc = bf16_bits_to_f64(np.asarray(vc_bits))
+    return attention_values(bf16_bits_to_f64(np.asarray(q_bits)),
+                            bf16_bits_to_f64(np.asarray(kc_bits)),
+                            bf16_bits_to_f64(np.asarray(vc_bits)),
+                            block_tables, qsl, ctx, seq_lens, scale)
+
+
+def attention_values(q, kc, vc, block_tables, qsl, ctx, seq_lens, scale):
+    """The same loops over float64 q [T,Hq,d] and caches [nb,Hkv,bs,d]."""
     T, hq, d = q.shape
     _, hkv, bs, _ = kc.shape
     per_kv = hq // hkv

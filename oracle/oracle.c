@@ -63,6 +63,79 @@ static int64_t cache_index(int64_t blk, int64_t head, int64_t off, int64_t dim,
 }
 
 /*
+ * FP8 KV cache (quantisation of the KV cache, [AI] §02 推理优化): elements are
+ * stored as OCP FP8 E4M3 ("e4m3fn") codes with one fp32 scale per kv head for
+ * K and one for V; an element's value is decode(code) * scale.
+ *
+ * E4M3 as defined by the format: sign bit, 4 exponent bits (bias 7), 3
+ * mantissa bits.  Exponent field 0 holds the subnormals m/8 * 2^-6; fields
+ * 1..15 hold (1 + m/8) * 2^(e-7), except S.1111.111, which is NaN.  There is
+ * no infinity; the largest finite magnitude is 1.75 * 2^8 = 448.
+ */
+static double e4m3_value(uint8_t code)
+{
+    int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double mag;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        mag = ldexp((double)m / 8.0, -6);
+    else
+        mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/*
+ * Encoding (a reading: the pages name FP8 KV caches without fixing the
+ * rounding): round to the nearest representable magnitude, ties to the even
+ * mantissa, and saturate magnitudes beyond 448 (including infinity) to 448.
+ * NaN encodes as 0x7F.
+ */
+static uint8_t e4m3_encode(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal grid: multiples of 2^-9; a result of 8 * 2^-9 = 2^-6 is
+         * the smallest normal, whose code (exponent 1, mantissa 0) is 8 too */
+        double q = nearbyint(ldexp(a, 9)); /* default rounding: ties to even */
+        return sign | (uint8_t)q;
+    }
+    int e = ilogb(a);                        /* 2^e <= a < 2^(e+1), -6 <= e <= 8 */
+    double q = nearbyint(ldexp(a, 3 - e));   /* in [8, 16] */
+    if (q == 16.0) {
+        q = 8.0;
+        e += 1;
+    }
+    if (e > 8 || (e == 8 && q > 14.0))
+        return sign | 0x7E;
+    return sign | (uint8_t)(((e + 7) << 3) | ((int)q - 8));
+}
+
+/* Array forms of the two conversions (pinned on their own by the tests). */
+int oracle_e4m3_encode(const float *x, int64_t n, uint8_t *codes)
+{
+    if (n < 0)
+        return ORC_BAD_ARG;
+    for (int64_t i = 0; i < n; ++i)
+        codes[i] = e4m3_encode(x[i]);
+    return ORC_OK;
+}
+
+int oracle_e4m3_decode(const uint8_t *codes, int64_t n, double *x)
+{
+    if (n < 0)
+        return ORC_BAD_ARG;
+    for (int64_t i = 0; i < n; ++i)
+        x[i] = e4m3_value(codes[i]);
+    return ORC_OK;
+}
+
+/*
  * reshape_and_cache: for every new token t with slot s = slot_mapping[t] >= 0,
  * cache[s / block_size][h][s % block_size][:] = k[t][h][:] (same for v).
  * Pure bit copy.  [CH] §11.2 (a token lands in a slot of a fixed-size block).
@@ -88,6 +161,41 @@ int oracle_write_kv(const uint16_t *k, const uint16_t *v, const int64_t *slot_ma
                 int64_t dst = cache_index(blk, h, off, e, num_kv_heads, block_size, head_dim);
                 k_cache[dst] = k[src];
                 v_cache[dst] = v[src];
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/*
+ * reshape_and_cache into an FP8 cache: the same slots as oracle_write_kv,
+ * each element stored as e4m3_encode(x / scale[h]), the quotient taken in
+ * binary32 (x is the bf16 value widened exactly; the division rounds to
+ * nearest even), then encoded as above.
+ */
+int oracle_write_kv_fp8(const uint16_t *k, const uint16_t *v, const int64_t *slot_mapping,
+                        int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t block_size, int32_t num_blocks, const float *k_scale,
+                        const float *v_scale, uint8_t *k_cache, uint8_t *v_cache)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
+        return ORC_BAD_ARG;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s < 0)
+            continue;
+        int64_t blk = s / block_size;
+        int64_t off = s % block_size;
+        if (blk >= num_blocks)
+            return ORC_BAD_META;
+        for (int64_t h = 0; h < num_kv_heads; ++h) {
+            for (int64_t e = 0; e < head_dim; ++e) {
+                int64_t src = (t * num_kv_heads + h) * head_dim + e;
+                int64_t dst = cache_index(blk, h, off, e, num_kv_heads, block_size, head_dim);
+                float kx = (float)bf16_value(k[src]), vx = (float)bf16_value(v[src]);
+                float kq = kx / k_scale[h], vq = vx / v_scale[h];
+                k_cache[dst] = e4m3_encode(kq);
+                v_cache[dst] = e4m3_encode(vq);
             }
         }
     }
@@ -132,10 +240,25 @@ static void attend_row(const double *qrow, const double *keys, const double *val
     *lse_out = lse;
 }
 
+/* The caches of one call: bf16 bit patterns, or e4m3 codes with per-kv-head
+ * scales. */
+typedef struct {
+    const void *k, *v;
+    const float *k_scale, *v_scale; /* fp8 only */
+    int fp8;
+} kv_source;
+
+static double kv_element(const kv_source *src, int is_v, int64_t idx, int32_t head)
+{
+    if (!src->fp8)
+        return bf16_value(((const uint16_t *)(is_v ? src->v : src->k))[idx]);
+    uint8_t code = ((const uint8_t *)(is_v ? src->v : src->k))[idx];
+    return e4m3_value(code) * (double)(is_v ? src->v_scale[head] : src->k_scale[head]);
+}
+
 /* Gather keys [0, len) of one kv head through a block table into dense
  * [len][head_dim] arrays.  [CH] §11.2: logical block j -> physical block. */
-static int gather_kv(const uint16_t *k_cache, const uint16_t *v_cache,
-                     const int32_t *table_row, int64_t len, int32_t head,
+static int gather_kv(const kv_source *src, const int32_t *table_row, int64_t len, int32_t head,
                      int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
                      int32_t head_dim, double *keys, double *vals)
 {
@@ -145,9 +268,9 @@ static int gather_kv(const uint16_t *k_cache, const uint16_t *v_cache,
         if (blk < 0 || blk >= num_blocks)
             return ORC_BAD_META;
         for (int32_t e = 0; e < head_dim; ++e) {
-            int64_t src = cache_index(blk, head, off, e, num_kv_heads, block_size, head_dim);
-            keys[j * head_dim + e] = bf16_value(k_cache[src]);
-            vals[j * head_dim + e] = bf16_value(v_cache[src]);
+            int64_t idx = cache_index(blk, head, off, e, num_kv_heads, block_size, head_dim);
+            keys[j * head_dim + e] = kv_element(src, 0, idx, head);
+            vals[j * head_dim + e] = kv_element(src, 1, idx, head);
         }
     }
     return ORC_OK;
@@ -166,12 +289,13 @@ static int gather_kv(const uint16_t *k_cache, const uint16_t *v_cache,
  * [num_q_tokens][num_q_heads]; visible (optional): int32 [num_q_tokens], the
  * number of keys each row attends to.
  */
-int oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
-                     int32_t num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
-                     const int32_t *block_tables, int32_t max_blocks_per_seq,
-                     const int32_t *query_start_loc, const int32_t *context_lens,
-                     const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
-                     double scale, double *out, double *lse, int32_t *visible)
+static int attention_impl(const uint16_t *q, const kv_source *src,
+                          int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                          int32_t head_dim, const int32_t *block_tables,
+                          int32_t max_blocks_per_seq, const int32_t *query_start_loc,
+                          const int32_t *context_lens, const int32_t *seq_lens, int32_t num_seqs,
+                          int32_t num_q_heads, double scale, double *out, double *lse,
+                          int32_t *visible)
 {
     if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_dim <= 0 ||
         block_size <= 0 || num_q_heads % num_kv_heads != 0)
@@ -207,7 +331,7 @@ int oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t 
             continue;
         }
         const int32_t *table_row = block_tables + (int64_t)b * max_blocks_per_seq;
-        if (gather_kv(k_cache, v_cache, table_row, len, hk, num_blocks, block_size,
+        if (gather_kv(src, table_row, len, hk, num_blocks, block_size,
                       num_kv_heads, head_dim, keys, vals) != ORC_OK) {
 #pragma omp atomic write
             status = ORC_BAD_META;
@@ -234,6 +358,35 @@ int oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t 
         free(keys); free(vals); free(scores); free(qrow);
     }
     return status;
+}
+
+int oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                     int32_t num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                     const int32_t *block_tables, int32_t max_blocks_per_seq,
+                     const int32_t *query_start_loc, const int32_t *context_lens,
+                     const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                     double scale, double *out, double *lse, int32_t *visible)
+{
+    kv_source src = {k_cache, v_cache, NULL, NULL, 0};
+    return attention_impl(q, &src, num_blocks, block_size, num_kv_heads, head_dim, block_tables,
+                          max_blocks_per_seq, query_start_loc, context_lens, seq_lens, num_seqs,
+                          num_q_heads, scale, out, lse, visible);
+}
+
+/* The same attention over an FP8 cache: every key and value element is
+ * decode(code) * scale[kv head], in fp64, before the plain definition. */
+int oracle_attention_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                         const float *k_scale, const float *v_scale, int32_t num_blocks,
+                         int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                         const int32_t *query_start_loc, const int32_t *context_lens,
+                         const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                         double scale, double *out, double *lse, int32_t *visible)
+{
+    kv_source src = {k_cache, v_cache, k_scale, v_scale, 1};
+    return attention_impl(q, &src, num_blocks, block_size, num_kv_heads, head_dim, block_tables,
+                          max_blocks_per_seq, query_start_loc, context_lens, seq_lens, num_seqs,
+                          num_q_heads, scale, out, lse, visible);
 }
 
 /*
@@ -265,7 +418,8 @@ int oracle_prefix_attention(const uint16_t *q, const uint16_t *k_cache, const ui
             free(keys); free(vals); free(scores); free(qrow);
             continue;
         }
-        if (gather_kv(k_cache, v_cache, prefix_blocks, prefix_len, hk, num_blocks, block_size,
+        kv_source src = {k_cache, v_cache, NULL, NULL, 0};
+        if (gather_kv(&src, prefix_blocks, prefix_len, hk, num_blocks, block_size,
                       num_kv_heads, head_dim, keys, vals) != ORC_OK) {
 #pragma omp atomic write
             status = ORC_BAD_META;

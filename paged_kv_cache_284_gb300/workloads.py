@@ -102,6 +102,44 @@ def _blocks_for(length: int, bs: int) -> int:
     return (length + bs - 1) // bs
 
 
+@dataclasses.dataclass
+class Fp8Pool:
+    """An e4m3 KV pool: uint8 codes [num_blocks, Hkv, bs, d] for K and V and
+    one fp32 scale per kv head for each (an element is code value x scale)."""
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    k_scale: torch.Tensor
+    v_scale: torch.Tensor
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.k_cache.shape[0])
+
+
+def _random_e4m3_codes(shape, gen: torch.Generator) -> torch.Tensor:
+    """Finite e4m3 codes with a random sign, an exponent field uniform in
+    1..11 (magnitudes 2^-6 .. 30) and a uniform mantissa: log-uniform values,
+    no NaN code."""
+    sign = torch.randint(0, 2, shape, generator=gen, dtype=torch.int32) << 7
+    e = torch.randint(1, 12, shape, generator=gen, dtype=torch.int32) << 3
+    m = torch.randint(0, 8, shape, generator=gen, dtype=torch.int32)
+    return (sign | e | m).to(torch.uint8)
+
+
+def fp8_pool_like(pool: Pool, seed: int) -> Fp8Pool:
+    """An e4m3 pool with the shape of `pool`: seeded random codes and per-kv-head
+    scales uniform in [1/24, 1/12] (so new bf16 N(0,1) tokens divided by the
+    scale stay far inside the e4m3 range)."""
+    gen = torch.Generator().manual_seed(seed)
+    shape = tuple(pool.k_cache.shape)
+    hkv = shape[1]
+    kc = _random_e4m3_codes(shape, gen)
+    vc = _random_e4m3_codes(shape, gen)
+    ks = 1.0 / torch.empty(hkv).uniform_(12.0, 24.0, generator=gen)
+    vs = 1.0 / torch.empty(hkv).uniform_(12.0, 24.0, generator=gen)
+    return Fp8Pool(kc, vc, ks.float(), vs.float())
+
+
 def make_pool(num_blocks: int, num_kv_heads: int, block_size: int, head_dim: int,
               gen: torch.Generator) -> Pool:
     shape = (num_blocks, num_kv_heads, block_size, head_dim)
