@@ -59,12 +59,30 @@ enum {
 #define PA_DEV_WAIT_TIMEOUT  0x8u  /* a pipeline wait ran out; the kernel stopped early    */
 #define PA_DEV_PLAN_OVERFLOW 0x10u /* work did not fit the workspace's item capacity       */
 
+/* Element type of a KV pool (pa_kv_desc.kv_dtype). */
+enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 };
+
 /*
  * The paged KV pool ([CH] §11.2): two arrays (K and V) of physical blocks,
- * each bf16 [num_blocks][num_kv_heads][block_size][head_dim], row-major, so
- * one (block, kv head) is block_size*head_dim contiguous elements.  Slot s
- * holds token offset s % block_size of physical block s / block_size.
- * Both pointers must be 16-byte aligned.
+ * each [num_blocks][num_kv_heads][block_size][head_dim], row-major, so one
+ * (block, kv head) is block_size*head_dim contiguous elements.  Slot s holds
+ * token offset s % block_size of physical block s / block_size.  Both
+ * pointers must be 16-byte aligned.
+ *
+ * kv_dtype PA_KV_BF16 (0, the default of a zeroed descriptor): bf16
+ * elements; k_scale / v_scale are ignored.
+ *
+ * kv_dtype PA_KV_FP8_E4M3: quantised KV cache (2048ai.net page on the vLLM V1
+ * engine, §02 推理优化: quantisation of the KV cache).  Elements are one-byte
+ * OCP FP8 E4M3 codes (bias 7, 3 mantissa bits, no infinity, largest finite
+ * 448, S.1111.111 = NaN); k_scale and v_scale are device fp32
+ * [num_kv_heads], and an element of kv head h stands for code * k_scale[h]
+ * (v_scale[h] for V).  The scales are the caller's; they must be finite and
+ * positive.  head_dim must be 128.  Attention over an fp8 pool computes q in
+ * f16 (|q| must stay below 65504), K and V as decoded exactly to f16 and
+ * scaled in fp32; all rows run on the split-KV kernel (longer requests in
+ * pieces of 64 / group query tokens).  pa_prefix_attention and
+ * pa_cascade_decode accept bf16 pools only.
  */
 typedef struct pa_kv_desc {
     void *k_cache;
@@ -73,15 +91,23 @@ typedef struct pa_kv_desc {
     int32_t block_size;
     int32_t num_kv_heads;
     int32_t head_dim;
+    int32_t kv_dtype;       /* PA_KV_BF16 or PA_KV_FP8_E4M3 */
+    int32_t reserved;       /* must be 0 */
+    const float *k_scale;   /* fp8 only: device fp32 [num_kv_heads] */
+    const float *v_scale;   /* fp8 only: device fp32 [num_kv_heads] */
 } pa_kv_desc;
 
 /*
  * reshape_and_cache: scatter this step's new K/V rows into their slots.
  * For every token t with s = slot_mapping[t] >= 0 and every kv head h:
  *   k_cache[s / bs][h][s % bs][:] = k[t][h][:]   (same for v)
- * Bit-exact copy.  Negative slots are skipped (padding).  A slot beyond the
- * pool is skipped and flags PA_DEV_BAD_SLOT.  Duplicate slots in one call
- * are invalid (which write wins is unspecified).
+ * bf16 pool: bit-exact copy.  fp8 pool: each element x becomes
+ * e4m3(x / k_scale[h]) (v_scale for v): the quotient in IEEE binary32,
+ * rounded to nearest even, then rounded to the nearest e4m3 value (ties to
+ * the even mantissa), magnitudes beyond 448 saturating to 448 (NaN stays
+ * NaN).  Negative slots are skipped (padding).  A slot beyond the pool is
+ * skipped and flags PA_DEV_BAD_SLOT.  Duplicate slots in one call are
+ * invalid (which write wins is unspecified).
  *   k, v          bf16 [num_tokens][num_kv_heads][head_dim], 16-B aligned
  *   slot_mapping  int64 [num_tokens]
  * Source: [CH] §11.2 (tokens fill fixed-size blocks allocated on demand);

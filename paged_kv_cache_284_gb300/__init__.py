@@ -49,10 +49,15 @@ _STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_
            4: "PA_ERR_CUDA", 5: "PA_ERR_BAD_METADATA"}
 
 
+PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
+
+
 class KVDesc(ctypes.Structure):
     _fields_ = [("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
                 ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
-                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
 
 
 def _declare(lib):
@@ -127,21 +132,45 @@ def _need(t: torch.Tensor, name: str, dtype, device=True):
         raise ValueError(f"{name} must be a CUDA tensor")
 
 
-def kv_desc(k_cache: torch.Tensor, v_cache: torch.Tensor) -> KVDesc:
-    _need(k_cache, "k_cache", torch.bfloat16)
-    _need(v_cache, "v_cache", torch.bfloat16)
+_FP8_DTYPES = (torch.uint8,) + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ())
+
+
+def kv_desc(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale=None, v_scale=None) -> KVDesc:
+    """Descriptor of a paged KV pool.  bf16 caches: k_scale / v_scale must be
+    None.  e4m3 caches (torch.uint8 codes or torch.float8_e4m3fn): k_scale and
+    v_scale are fp32 CUDA tensors [num_kv_heads]."""
+    if k_cache.dtype in _FP8_DTYPES:
+        for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+            if t.dtype not in _FP8_DTYPES or not t.is_contiguous() or not t.is_cuda:
+                raise TypeError(f"{name} must be a contiguous CUDA uint8 / float8_e4m3fn tensor")
+        if k_scale is None or v_scale is None:
+            raise ValueError("an fp8 KV pool needs k_scale and v_scale")
+        _need(k_scale, "k_scale", torch.float32)
+        _need(v_scale, "v_scale", torch.float32)
+        dtype = PA_KV_FP8_E4M3
+    else:
+        _need(k_cache, "k_cache", torch.bfloat16)
+        _need(v_cache, "v_cache", torch.bfloat16)
+        if k_scale is not None or v_scale is not None:
+            raise ValueError("scales are for fp8 KV pools only")
+        dtype = PA_KV_BF16
     if k_cache.shape != v_cache.shape or k_cache.dim() != 4:
         raise ValueError("caches must both be [num_blocks, num_kv_heads, block_size, head_dim]")
     nb, hkv, bs, d = k_cache.shape
-    return KVDesc(k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, hkv, d)
+    if dtype == PA_KV_FP8_E4M3 and (k_scale.numel() != hkv or v_scale.numel() != hkv):
+        raise ValueError("k_scale / v_scale must hold num_kv_heads values")
+    return KVDesc(k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, hkv, d, dtype, 0,
+                  None if k_scale is None else k_scale.data_ptr(),
+                  None if v_scale is None else v_scale.data_ptr())
 
 
-def pa_write_kv(k, v, slot_mapping, k_cache, v_cache, stream=None):
-    """reshape_and_cache: k/v bf16 [T, Hkv, d], slot_mapping int64 [T]."""
+def pa_write_kv(k, v, slot_mapping, k_cache, v_cache, stream=None, k_scale=None, v_scale=None):
+    """reshape_and_cache: k/v bf16 [T, Hkv, d], slot_mapping int64 [T]; an fp8
+    pool quantises with k_scale / v_scale (fp32 [Hkv])."""
     _need(k, "k", torch.bfloat16)
     _need(v, "v", torch.bfloat16)
     _need(slot_mapping, "slot_mapping", torch.int64)
-    kv = kv_desc(k_cache, v_cache)
+    kv = kv_desc(k_cache, v_cache, k_scale, v_scale)
     _check(lib().pa_write_kv(_ptr(k), _ptr(v), _ptr(slot_mapping), int(k.shape[0]),
                              ctypes.byref(kv), _stream(stream)), "pa_write_kv")
 
@@ -164,9 +193,10 @@ def alloc_workspace(nbytes: int, device=None) -> torch.Tensor:
 
 def pa_attention(q, k_cache, v_cache, block_tables, query_start_loc, context_lens, seq_lens,
                  scale, out, lse=None, workspace=None, stream=None, short_q_max_rows=-1,
-                 split_keys=0):
+                 split_keys=0, k_scale=None, v_scale=None):
     """Varlen paged attention for one step; writes out (bf16 [T,Hq,d]) and lse
-    (fp32 [T,Hq], optional).  Returns the workspace tensor used."""
+    (fp32 [T,Hq], optional).  An fp8 pool takes k_scale / v_scale (fp32
+    [Hkv]).  Returns the workspace tensor used."""
     _need(q, "q", torch.bfloat16)
     _need(out, "out", torch.bfloat16)
     for name, t in (("block_tables", block_tables), ("query_start_loc", query_start_loc),
@@ -174,7 +204,7 @@ def pa_attention(q, k_cache, v_cache, block_tables, query_start_loc, context_len
         _need(t, name, torch.int32)
     if lse is not None:
         _need(lse, "lse", torch.float32)
-    kv = kv_desc(k_cache, v_cache)
+    kv = kv_desc(k_cache, v_cache, k_scale, v_scale)
     T, hq, _ = q.shape
     B = int(seq_lens.shape[0])
     need = workspace_size(B, T, hq, kv.num_kv_heads, kv.head_dim)
@@ -271,7 +301,8 @@ def set_profile_events(which: int, start=None, end=None):
 
 
 def pa_attention_no_alloc(q, k_cache, v_cache, block_tables, query_start_loc, context_lens,
-                          seq_lens, scale, out, lse=None, stream=None):
+                          seq_lens, scale, out, lse=None, stream=None, k_scale=None,
+                          v_scale=None):
     """pa_attention without a workspace, for callers that cannot allocate
     device memory: the library's own fixed scratch array is used.  Calls that
     overlap on the GPU share that array and must be ordered."""
@@ -282,7 +313,7 @@ def pa_attention_no_alloc(q, k_cache, v_cache, block_tables, query_start_loc, co
         _need(t, name, torch.int32)
     if lse is not None:
         _need(lse, "lse", torch.float32)
-    kv = kv_desc(k_cache, v_cache)
+    kv = kv_desc(k_cache, v_cache, k_scale, v_scale)
     T, hq, _ = q.shape
     _check(lib().pa_attention_no_alloc(_ptr(q), ctypes.byref(kv), _ptr(block_tables),
                                        int(block_tables.shape[1]), _ptr(query_start_loc),

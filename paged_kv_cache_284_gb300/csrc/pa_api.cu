@@ -37,7 +37,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
     bool ready = false;
     int sms = 0;
-    int short_ctas_per_sm[2] = {0, 0};  // head_dim 64, 128
+    int short_ctas_per_sm[3] = {0, 0, 0};  // bf16 head_dim 64, bf16 128, fp8 128
     unsigned *status = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -56,8 +56,9 @@ int device_info(DeviceInfo **out) {
         d.status = static_cast<unsigned *>(sym);
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return fail(PA_ERR_CUDA, "cannot query SM count");
-        d.short_ctas_per_sm[0] = short_max_ctas_per_sm(64);
-        d.short_ctas_per_sm[1] = short_max_ctas_per_sm(128);
+        d.short_ctas_per_sm[0] = short_max_ctas_per_sm(64, false);
+        d.short_ctas_per_sm[1] = short_max_ctas_per_sm(128, false);
+        d.short_ctas_per_sm[2] = short_max_ctas_per_sm(128, true);
         d.ready = true;
     }
     *out = &d;
@@ -79,15 +80,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D view of one cache array: rows = (block, kv head, offset) flattened,
-// head_dim columns; boxes of 16 rows x 64 columns, 128-byte swizzle.
-int make_kv_map(CUtensorMap *m, void *base, int64_t rows, int head_dim) {
+// head_dim columns; boxes of 16 rows x 128 bytes (64 bf16 or 128 e4m3
+// columns), 128-byte swizzle.
+int make_kv_map(CUtensorMap *m, void *base, int64_t rows, int head_dim, bool fp8) {
     auto fn = encode_fn();
     if (!fn) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    const int esize = fp8 ? 1 : 2;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kChunkKeys)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * esize};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), static_cast<cuuint32_t>(kChunkKeys)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+    CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    base, dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : fail(PA_ERR_CUDA, "KV tensor map encode failed (%d)", (int)r);
@@ -137,16 +141,25 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 int q_tile_tokens(int group) { return group <= kLongRows ? kLongRows / group : 0; }
 
+// Query tokens per split-KV piece (a piece fills at most kShortMaxRows rows),
+// and a bound on the pieces of a step with these sizes.
+int piece_tokens_for(int group) { return std::max(1, kShortMaxRows / std::max(1, group)); }
+int pieces_bound(int num_seqs, int num_q_tokens, int group) {
+    const int pt = piece_tokens_for(group);
+    return num_seqs + (num_q_tokens + pt - 1) / pt;
+}
+
 WsLayout make_layout(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads,
                      int head_dim, int prefix_partial_rows, bool with_extra) {
     WsLayout L{};
     const int group = num_q_heads / num_kv_heads;
     const int tq = q_tile_tokens(group);
-    L.max_short = num_kv_heads * num_seqs * 8 + 4096;
+    const int pieces = pieces_bound(num_seqs, num_q_tokens, group);
+    L.max_short = num_kv_heads * (num_seqs * 8 + pieces) + 4096;
     L.max_long = num_kv_heads * ((num_q_tokens + tq - 1) / tq + num_seqs);
-    L.cap_rows = L.max_short * 8;
+    L.cap_rows = L.max_short * 4;
     if (prefix_partial_rows > L.cap_rows) L.cap_rows = prefix_partial_rows;
-    L.num_counters = num_kv_heads * (num_seqs > 0 ? num_seqs : 1);
+    L.num_counters = num_kv_heads * std::max(1, pieces);
     const int prefix_counters = num_kv_heads * ((num_q_tokens + tq - 1) / tq + 1);
     if (with_extra && prefix_counters > L.num_counters) L.num_counters = prefix_counters;
     size_t off = 0;
@@ -187,6 +200,15 @@ int check_kv(const pa_kv_desc *kv) {
     if (kv->block_size <= 0 || kv->block_size % 16 != 0 || kv->block_size > 256)
         return fail(PA_ERR_UNSUPPORTED, "block_size %d: need a multiple of 16, at most 256",
                     kv->block_size);
+    if (kv->reserved != 0) return fail(PA_ERR_INVALID_ARG, "pa_kv_desc.reserved must be 0");
+    if (kv->kv_dtype == PA_KV_FP8_E4M3) {
+        if (kv->head_dim != 128)
+            return fail(PA_ERR_UNSUPPORTED, "fp8 KV pool: head_dim %d not built (128)", kv->head_dim);
+        if (!kv->k_scale || !kv->v_scale || !aligned(kv->k_scale, 4) || !aligned(kv->v_scale, 4))
+            return fail(PA_ERR_INVALID_ARG, "fp8 KV pool needs 4-byte aligned k_scale and v_scale");
+    } else if (kv->kv_dtype != PA_KV_BF16) {
+        return fail(PA_ERR_UNSUPPORTED, "kv_dtype %d unknown", kv->kv_dtype);
+    }
     const int64_t rows = static_cast<int64_t>(kv->num_blocks) * kv->num_kv_heads * kv->block_size;
     if (rows >= (static_cast<int64_t>(1) << 31) - 256)
         return fail(PA_ERR_UNSUPPORTED, "pool too large: %lld cache rows", (long long)rows);
@@ -213,8 +235,9 @@ struct StepMaps {
 
 int make_maps(StepMaps *m, const void *q, const pa_kv_desc *kv, int tokens, int heads) {
     const int group = heads / kv->num_kv_heads;
-    int rc = make_kv_map(&m->k, kv->k_cache, kv_rows(kv), kv->head_dim);
-    if (rc == PA_OK) rc = make_kv_map(&m->v, kv->v_cache, kv_rows(kv), kv->head_dim);
+    const bool fp8 = kv->kv_dtype == PA_KV_FP8_E4M3;
+    int rc = make_kv_map(&m->k, kv->k_cache, kv_rows(kv), kv->head_dim, fp8);
+    if (rc == PA_OK) rc = make_kv_map(&m->v, kv->v_cache, kv_rows(kv), kv->head_dim, fp8);
     if (rc == PA_OK)
         rc = make_q_map(&m->q, q, tokens, heads, kv->head_dim, group, q_tile_tokens(group));
     return rc;
@@ -242,9 +265,14 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
     pp.num_kv_heads = kv->num_kv_heads;
     pp.group = group;
     pp.q_tile_tokens = tq;
+    // an fp8 pool runs every row on the split-KV kernel; a request longer
+    // than a piece is cut into pieces of piece_tokens query tokens
+    const bool fp8 = kv->kv_dtype == PA_KV_FP8_E4M3;
+    if (fp8) forbid_long = true;
     pp.short_max_rows = forbid_long ? 0x7fffffff : short_max_rows;
+    pp.piece_tokens = std::max(1, std::min(pp.short_max_rows, kShortMaxRows) / group);
     pp.split_stages = split_keys / kStageKeys;
-    const int short_grid = dev->sms * dev->short_ctas_per_sm[D == 128 ? 1 : 0];
+    const int short_grid = dev->sms * dev->short_ctas_per_sm[fp8 ? 2 : (D == 128 ? 1 : 0)];
     pp.target_items = kSplitItemsPerCta * short_grid;
     pp.hdr = hdr;
     pp.short_items = reinterpret_cast<ShortItem *>(ws + L.short_items);
@@ -285,10 +313,12 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
     sp.partial_lse = reinterpret_cast<float *>(ws + L.partial_lse);
     sp.extra_o = extra_o;
     sp.extra_lse = extra_lse;
+    sp.k_scale = fp8 ? kv->k_scale : nullptr;
+    sp.v_scale = fp8 ? kv->v_scale : nullptr;
     sp.status = dev->status;
     {
         ProfScope prof(PA_KERNEL_SPLIT_KV, s);
-        rc = launch_short(sp, maps.k, maps.v, D, short_grid, s);
+        rc = launch_short(sp, maps.k, maps.v, D, fp8, short_grid, s);
     }
     if (rc != PA_OK) return fail(rc, "split-KV kernel launch failed: %s",
                                  cudaGetErrorString(cudaGetLastError()));
@@ -348,6 +378,9 @@ int common_checks(const void *q, const pa_kv_desc *kv, int32_t num_q_tokens, int
     if (!aligned(q, 16) || !aligned(out, 16))
         return fail(PA_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
     if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale is not finite");
+    if (kv->kv_dtype == PA_KV_FP8_E4M3 && num_q_heads / kv->num_kv_heads > kShortMaxRows)
+        return fail(PA_ERR_UNSUPPORTED, "fp8 KV pool: group size above %d not built",
+                    kShortMaxRows);
     if (workspace && !aligned(workspace, 256))
         return fail(PA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
     return PA_OK;
@@ -444,9 +477,10 @@ int attention_in_fixed_workspace(const void *q, const pa_kv_desc *kv,
     const int hkv = kv->num_kv_heads, D = kv->head_dim;
     const int tq = q_tile_tokens(num_q_heads / hkv);
     WsLayout L{};
-    L.max_short = hkv * num_seqs + 4096;
+    const int pieces = pieces_bound(num_seqs, num_q_tokens, num_q_heads / hkv);
+    L.max_short = hkv * pieces + 4096;
     L.max_long = hkv * ((num_q_tokens + tq - 1) / tq + num_seqs);
-    L.num_counters = hkv * num_seqs;
+    L.num_counters = hkv * pieces;
     size_t off = 0;
     L.header = off;
     off = align256(off + sizeof(PlanHeader));
@@ -605,6 +639,8 @@ int pa_prefix_attention(const void *q, const pa_kv_desc *kv, const int32_t *pref
     g_err[0] = 0;
     int rc = common_checks(q, kv, num_q_tokens, num_q_heads, scale, out, workspace);
     if (rc != PA_OK) return rc;
+    if (kv->kv_dtype != PA_KV_BF16)
+        return fail(PA_ERR_UNSUPPORTED, "prefix attention is built for bf16 KV pools only");
     if (prefix_len < 0) return fail(PA_ERR_INVALID_ARG, "prefix_len < 0");
     if (prefix_len > 0 && !prefix_blocks) return fail(PA_ERR_INVALID_ARG, "prefix_blocks is NULL");
     if (num_q_tokens == 0) return PA_OK;
@@ -634,6 +670,11 @@ int pa_cascade_decode(const void *q, const pa_kv_desc *kv, const int32_t *prefix
     g_err[0] = 0;
     int rc = common_checks(q, kv, num_q_tokens, num_q_heads, scale, out, workspace);
     if (rc != PA_OK) return rc;
+    if (kv->kv_dtype != PA_KV_BF16)
+        return fail(PA_ERR_UNSUPPORTED, "cascade decode is built for bf16 KV pools only");
+    if (num_q_heads / kv->num_kv_heads > kShortMaxRows)
+        return fail(PA_ERR_UNSUPPORTED, "cascade decode: group size above %d not built",
+                    kShortMaxRows);
     if (num_seqs < 0 || prefix_len < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
     if (prefix_len > 0 && !prefix_blocks) return fail(PA_ERR_INVALID_ARG, "prefix_blocks is NULL");
     if (num_seqs == 0 || num_q_tokens == 0) return PA_OK;

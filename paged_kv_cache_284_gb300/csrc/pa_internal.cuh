@@ -54,14 +54,17 @@ static_assert(sizeof(PlanHeader) == 64, "header size");
 // writes one 32-byte record (two 16-byte stores) per request split or query
 // tile instead of one per kv head.
 
-// Split-KV record: request b, keys [stage_begin*64, min(stage_end*64, seq_len)).
-// Split s of kv head h writes partial rows partial_base + h*nsplit*R + [0, R)
-// (R = q_len * group) when nsplit > 1.
+// Split-KV record: query tokens [q_begin, q_begin + q_count) of request b
+// (a whole short request, or one piece of a longer one), keys
+// [stage_begin*64, min(stage_end*64, seq_len)).  Split s of kv head h writes
+// partial rows partial_base + h*nsplit*R + [0, R) (R = q_count * group) when
+// nsplit > 1, and counts its completion in counters[counter*Hkv + h].
 struct alignas(16) ShortItem {
     int b, split, nsplit, stage_begin;
-    int stage_end, partial_base, pad0, pad1;
+    int stage_end, partial_base, q_begin, q_count;
+    int counter, pad0, pad1, pad2;
 };
-static_assert(sizeof(ShortItem) == 32, "item size");
+static_assert(sizeof(ShortItem) == 48, "item size");
 
 // Tensor-core record: query tile q_tile of request b (tile = 128/group tokens
 // x group heads), keys [key_begin, key_end).
@@ -76,18 +79,20 @@ static_assert(sizeof(LongItem) == 32, "item size");
 // concurrently with this grid's launch).
 template <typename T>
 __device__ __forceinline__ T load_record(const T *base, int rec) {
-    static_assert(sizeof(T) == 32, "record size");
+    static_assert(sizeof(T) % 16 == 0, "record size");
     T r;
     const int4 *src = reinterpret_cast<const int4 *>(base + rec);
-    *reinterpret_cast<int4 *>(&r) = __ldcg(src);
-    *(reinterpret_cast<int4 *>(&r) + 1) = __ldcg(src + 1);
+#pragma unroll
+    for (int i = 0; i < static_cast<int>(sizeof(T) / 16); ++i)
+        reinterpret_cast<int4 *>(&r)[i] = __ldcg(src + i);
     return r;
 }
 template <typename T>
 __device__ __forceinline__ void store_record(T *base, int rec, const T &r) {
     int4 *dst = reinterpret_cast<int4 *>(base + rec);
-    dst[0] = *reinterpret_cast<const int4 *>(&r);
-    dst[1] = *(reinterpret_cast<const int4 *>(&r) + 1);
+#pragma unroll
+    for (int i = 0; i < static_cast<int>(sizeof(T) / 16); ++i)
+        dst[i] = reinterpret_cast<const int4 *>(&r)[i];
 }
 #endif
 
@@ -113,6 +118,7 @@ struct ShortParams {
     int *counters;
     float *partial_o, *partial_lse;
     const float *extra_o, *extra_lse;  // cascade: prefix state folded into the output
+    const float *k_scale, *v_scale;    // fp8 pool: per-kv-head dequantisation scales
     unsigned *status;
 };
 
@@ -144,6 +150,7 @@ struct PlanParams {
     const int *qsl, *ctx, *seq_lens;
     int num_seqs, num_q_tokens, num_kv_heads, group, q_tile_tokens;
     int short_max_rows;  // q_len*group <= this -> split-KV kernel
+    int piece_tokens;    // a split-KV request is cut into pieces of this many tokens
     int split_stages;    // 0 = automatic
     int target_items;    // automatic split aims at about this many split-KV items
     PlanHeader *hdr;
@@ -180,8 +187,8 @@ int launch_write_kv(const void *k, const void *v, const int64_t *slots, int num_
                     const pa_kv_desc *kv, unsigned *status, cudaStream_t s);
 int launch_plan(const PlanParams &p, cudaStream_t s);
 int launch_short(const ShortParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                 int head_dim, int grid, cudaStream_t s);
-int short_max_ctas_per_sm(int head_dim);
+                 int head_dim, bool fp8, int grid, cudaStream_t s);
+int short_max_ctas_per_sm(int head_dim, bool fp8);
 int launch_long(const LongParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                 const CUtensorMap &tv, int head_dim, int grid, cudaStream_t s);
 int launch_merge(const void *oa, const float *la, const void *ob, const float *lb, int n,
@@ -352,6 +359,41 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// f16 forms for the fp8 KV pool: K/V codes decode exactly to f16.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// lo -> bits 0..15, hi -> bits 16..31
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// two bf16 (lo, hi halves of v) -> two f16, same positions
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+    return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+// two e4m3 codes (byte 0 -> bits 0..15, byte 1 -> bits 16..31 of the result);
+// exact: every e4m3 value is an f16 value
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+        : "=r"(r)
+        : "r"(two_codes));
+    return r;
+}
+__device__ __forceinline__ uint32_t byte_perm(uint32_t x, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(x), "r"(sel));
+    return r;
 }
 
 // tcgen05 / TMEM -------------------------------------------------------------

@@ -65,8 +65,8 @@ __device__ long long block_sum_ll(long long v, long long *tmp) {
 struct ReqInfo {
     int n, ctx, len;
     int is_short;
-    int stages;   // 64-key stages of a short request
-    int qtiles;   // query tiles of a long request
+    int pieces;   // query pieces of a split-KV request
+    int qtiles;   // query tiles of a tensor-core request
 };
 
 __device__ __forceinline__ ReqInfo load_req(const PlanParams &p, int b) {
@@ -82,13 +82,26 @@ __device__ __forceinline__ ReqInfo load_req(const PlanParams &p, int b) {
         r.n = 0;
     }
     if (r.n > 0) {
-        r.is_short = (r.n * p.group <= p.short_max_rows) ? 1 : 0;
+        r.is_short = (static_cast<long long>(r.n) * p.group <= p.short_max_rows) ? 1 : 0;
         if (r.is_short)
-            r.stages = (r.len + kStageKeys - 1) / kStageKeys;
+            r.pieces = (r.n + p.piece_tokens - 1) / p.piece_tokens;
         else
             r.qtiles = (r.n + p.q_tile_tokens - 1) / p.q_tile_tokens;
     }
     return r;
+}
+
+// Piece i of a split-KV request: its query tokens and the 64-key stages up
+// to its last token's causal limit.
+struct Piece {
+    int q_begin, q_count, stages;
+};
+__device__ __forceinline__ Piece piece_of(const PlanParams &p, const ReqInfo &r, int i) {
+    Piece pc;
+    pc.q_begin = i * p.piece_tokens;
+    pc.q_count = min(p.piece_tokens, r.n - pc.q_begin);
+    pc.stages = (r.ctx + pc.q_begin + pc.q_count + kStageKeys - 1) / kStageKeys;
+    return pc;
 }
 
 constexpr int kSortBins = kPlanThreads;  // bins of the longest-first sort
@@ -135,17 +148,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
 
     // 1. total split-KV work (in stages) -------------------------------------
     long long work = 0;
-    int max_stages = 0;
+    int max_stages = 0, pieces = 0;
     for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
         const ReqInfo r = req(b);
-        if (r.is_short) {
-            work += r.stages;
-            max_stages = max(max_stages, r.stages);
+        for (int i = 0; i < r.pieces; ++i) {
+            const Piece pc = piece_of(p, r, i);
+            work += pc.stages;
+            max_stages = max(max_stages, pc.stages);
         }
+        pieces += r.pieces;
     }
     max_stages = __reduce_max_sync(0xffffffffu, max_stages);
     if (lane == 0 && max_stages > 0) atomicMax(&s_max_stages, max_stages);
     const long long total_work = block_sum_ll(work, tmpl) * hkv;  // also orders the atomics
+    const long long total_pieces = block_sum_ll(pieces, tmpl);
 
     // 2. split size ------------------------------------------------------------
     int sp;
@@ -160,34 +176,41 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         long long items = 0, rows = 0;
         for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
             const ReqInfo r = req(b);
-            if (!r.is_short) continue;
-            const int ns = (r.stages + sp - 1) / sp;
-            items += ns;
-            if (ns > 1) rows += static_cast<long long>(ns) * r.n * p.group;
+            for (int i = 0; i < r.pieces; ++i) {
+                const Piece pc = piece_of(p, r, i);
+                const int ns = (pc.stages + sp - 1) / sp;
+                items += ns;
+                if (ns > 1) rows += static_cast<long long>(ns) * pc.q_count * p.group;
+            }
         }
         items = block_sum_ll(items, tmpl) * hkv;
         rows = block_sum_ll(rows, tmpl) * hkv;
         if ((items <= p.max_short && rows <= p.cap_rows) || sp >= s_max_stages) break;
         sp *= 2;
     }
-    if (tid == 0) s_split = sp;
+    if (tid == 0) {
+        s_split = sp;
+        if (total_pieces * hkv > p.num_counters) s_overflow = 1;
+    }
     __syncthreads();
     sp = s_split;
 
-    int short_base = 0, long_base = 0, row_base = 0;
+    int short_base = 0, long_base = 0, row_base = 0, piece_base = 0;
 
     // 3. split-KV items, longest key range first (counting sort on the number
-    // of stages of the item).  A request's ns splits cut its stages into
-    // ranges that differ by at most one stage.  Partial-state rows are
-    // handed out in request order by a block scan.
+    // of stages of the item).  A piece's ns splits cut its stages into ranges
+    // that differ by at most one stage.  Partial-state rows and completion
+    // counters are handed out in request order by block scans.
     for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
         const ReqInfo r = req(b);
-        if (!r.is_short) continue;
-        const int ns = (r.stages + sp - 1) / sp;
-        for (int s = 0; s < ns; ++s)
-            atomicAdd(&bins[short_bin(split_begin(r.stages, ns, s + 1) -
-                                      split_begin(r.stages, ns, s))],
-                      1);
+        for (int i = 0; i < r.pieces; ++i) {
+            const Piece pc = piece_of(p, r, i);
+            const int ns = (pc.stages + sp - 1) / sp;
+            for (int s = 0; s < ns; ++s)
+                atomicAdd(&bins[short_bin(split_begin(pc.stages, ns, s + 1) -
+                                          split_begin(pc.stages, ns, s))],
+                          1);
+        }
     }
     __syncthreads();
     {
@@ -202,27 +225,44 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         const int b = b0 + tid;
         ReqInfo r{};
         if (b < p.num_seqs) r = req(b);
-        const int ns = r.is_short ? (r.stages + sp - 1) / sp : 0;
-        const int R = r.n * p.group;
-        const int n_rows = (ns > 1) ? ns * R * hkv : 0;
-        int tot_r;
-        const int off_r = row_base + block_exclusive_scan(n_rows, tmp, &tot_r);
-        row_base += tot_r;
-        if (static_cast<long long>(short_base) * hkv > p.max_short || row_base > p.cap_rows) {
-            if (tid == 0) s_overflow = 1;
-            continue;  // uniform: both totals are block-wide
+        int n_rows = 0;
+        for (int i = 0; i < r.pieces; ++i) {
+            const Piece pc = piece_of(p, r, i);
+            const int ns = (pc.stages + sp - 1) / sp;
+            if (ns > 1) n_rows += ns * pc.q_count * p.group * hkv;
         }
-        for (int s = 0; s < ns; ++s) {
-            const int s0 = split_begin(r.stages, ns, s), s1 = split_begin(r.stages, ns, s + 1);
-            ShortItem it;
-            it.b = b;
-            it.split = s;
-            it.nsplit = ns;
-            it.stage_begin = s0;
-            it.stage_end = s1;
-            it.partial_base = (ns > 1) ? off_r + s * R : 0;
-            it.pad0 = it.pad1 = 0;
-            store_record(p.short_items, atomicAdd(&bins[short_bin(s1 - s0)], 1), it);
+        int tot_r, tot_p;
+        const int off_r = row_base + block_exclusive_scan(n_rows, tmp, &tot_r);
+        const int off_p = piece_base + block_exclusive_scan(r.pieces, tmp, &tot_p);
+        row_base += tot_r;
+        piece_base += tot_p;
+        if (static_cast<long long>(short_base) * hkv > p.max_short || row_base > p.cap_rows ||
+            s_overflow) {
+            if (tid == 0) s_overflow = 1;
+            continue;  // uniform: the totals are block-wide and s_overflow was set before a barrier
+        }
+        int row = off_r;
+        for (int i = 0; i < r.pieces; ++i) {
+            const Piece pc = piece_of(p, r, i);
+            const int ns = (pc.stages + sp - 1) / sp;
+            const int R = pc.q_count * p.group;
+            for (int s = 0; s < ns; ++s) {
+                const int s0 = split_begin(pc.stages, ns, s);
+                const int s1 = split_begin(pc.stages, ns, s + 1);
+                ShortItem it;
+                it.b = b;
+                it.split = s;
+                it.nsplit = ns;
+                it.stage_begin = s0;
+                it.stage_end = s1;
+                it.partial_base = (ns > 1) ? row + s * R : 0;
+                it.q_begin = pc.q_begin;
+                it.q_count = pc.q_count;
+                it.counter = off_p + i;
+                it.pad0 = it.pad1 = it.pad2 = 0;
+                store_record(p.short_items, atomicAdd(&bins[short_bin(s1 - s0)], 1), it);
+            }
+            if (ns > 1) row += ns * R * hkv;
         }
     }
     __syncthreads();

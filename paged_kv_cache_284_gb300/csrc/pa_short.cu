@@ -21,23 +21,39 @@
 //    folds them with the merge operator (2048ai.net page on the vLLM V1
 //    engine, §02.1 级联推理) -- the fused split-KV epilogue.  A cascade prefix
 //    state can be folded in the same epilogue.
+//  * FP8 pool (same page, §02 推理优化: KV-cache quantisation): K and V are
+//    e4m3 codes, one 16-key x 128-dim TMA box per chunk (half the bytes of
+//    bf16).  The MMAs run in f16: e4m3 decodes exactly to f16, q is
+//    converted once per item, P is packed as f16.  K fragments come from
+//    plain ldmatrix (each lane gets 4 consecutive dims of one key; q's dims
+//    are permuted the same way inside each 16-dim k-step, which leaves the
+//    dot products unchanged).  V fragments come from ldmatrix.trans over dim
+//    pairs and a byte permute: each lane gets 2 keys x 2 dims, so the two
+//    dims of a pair land in two different 8-column output tiles; the output
+//    columns are permuted back when they are written.  Scores are scaled by
+//    the kv head's K scale, outputs by its V scale.
 #include "pa_internal.cuh"
 
 namespace pa {
 
 namespace {
 
-template <int D>
+template <int D, bool FP8>
 struct ShortGeom {
-    static constexpr int kHalves = D / 64;                    // 64-dim TMA boxes per row
+    static_assert(!FP8 || D == 128, "the fp8 pool is built for head_dim 128");
+    static constexpr int kHalves = FP8 ? 1 : D / 64;          // TMA boxes per 16-key chunk
     static constexpr int kBoxBytes = kChunkKeys * 128;        // 16 rows x 128 B
     static constexpr int kChunkBytes = kHalves * kBoxBytes;   // one 16-key chunk of K (or V)
     static constexpr int kStageBytes = 2 * kStageChunks * kChunkBytes;
-    static constexpr int kCtlBytes = 256;
-    static constexpr int kSmemBytes = kShortStages * kStageBytes + kCtlBytes + 1024;
-    // merge scratch (per writer warp): 16 rows x D floats + 16 m + 16 l
+    static constexpr int kStages = FP8 ? 5 : kShortStages;  // ring depth
+    // merge scratch (per writer warp): 16 rows x D floats + 16 m + 16 l; the
+    // bf16 ring is large enough to hold it in the stage being released, the
+    // fp8 ring is not and gets an area of its own
     static constexpr int kScratchFloats = 16 * D + 32;
-    static_assert(3 * kScratchFloats * 4 <= kStageBytes, "merge scratch must fit one stage");
+    static constexpr int kScratchBytes = FP8 ? 3 * kScratchFloats * 4 : 0;
+    static constexpr int kCtlBytes = 512;
+    static constexpr int kSmemBytes = kStages * kStageBytes + kScratchBytes + kCtlBytes + 1024;
+    static_assert(FP8 || 3 * kScratchFloats * 4 <= kStageBytes, "merge scratch must fit one stage");
 };
 
 struct StageMeta {
@@ -64,12 +80,12 @@ __device__ __forceinline__ uint32_t keep_pair(uint32_t v, bool lo, bool hi) {
 
 template <int D>
 struct Consumer {
-    using G = ShortGeom<D>;
     static constexpr int NT = D / 8;   // 8-wide output column tiles
     static constexpr int KS = D / 16;  // 16-deep k steps over the head dim
 
     // item-wide
-    int b, h, tok0, ctx, key_end, R, KQ, rt, kq, nsplit, split, partial_base;
+    int b, h, tok0, ctx, key_end, R, KQ, rt, kq, nsplit, split, partial_base, counter;
+    float sl2, vsc;  // score scale (log2 units) and value scale
     bool active;
     // per thread: rows g and g+8 of this warp's 16-row tile
     int limit0, limit1;
@@ -108,25 +124,28 @@ __device__ __forceinline__ ShortItem short_work(const ShortParams &p, int idx, i
 
 }  // namespace
 
-template <int D>
+template <int D, bool FP8>
 __global__ void __launch_bounds__(kShortThreads, 2)
     short_kernel(const ShortParams p, const __grid_constant__ CUtensorMap tmk,
                  const __grid_constant__ CUtensorMap tmv) {
-    using G = ShortGeom<D>;
+    using G = ShortGeom<D, FP8>;
+    constexpr int kStages = G::kStages;
     constexpr int NT = D / 8, KS = D / 16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *stage_mem = smem;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kShortStages * G::kStageBytes);
-    uint64_t *empty = full + kShortStages;
-    StageMeta *meta = reinterpret_cast<StageMeta *>(empty + kShortStages);
-    int *ctl = reinterpret_cast<int *>(meta + kShortStages);
+    float *own_scratch = reinterpret_cast<float *>(smem + kStages * G::kStageBytes);
+    uint64_t *full =
+        reinterpret_cast<uint64_t *>(smem + kStages * G::kStageBytes + G::kScratchBytes);
+    uint64_t *empty = full + kStages;
+    StageMeta *meta = reinterpret_cast<StageMeta *>(empty + kStages);
+    int *ctl = reinterpret_cast<int *>(meta + kStages);
     volatile int *abort_flag = ctl;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kShortStages; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kShortConsumerWarps);
         }
@@ -173,11 +192,11 @@ __global__ void __launch_bounds__(kShortThreads, 2)
         }
         while (!aborted) {
             if (cur_idx >= num_items) {
-                const int slot = it % kShortStages;
+                const int slot = it % kStages;
                 bool ok = true;
                 if (lane == 0) {
-                    if (it >= kShortStages)
-                        ok = mbar_wait(&empty[slot], ((it / kShortStages) - 1) & 1, abort_flag);
+                    if (it >= kStages)
+                        ok = mbar_wait(&empty[slot], ((it / kStages) - 1) & 1, abort_flag);
                     if (ok) {
                         meta[slot].item = -1;
                         mbar_arrive(&full[slot]);
@@ -202,10 +221,10 @@ __global__ void __launch_bounds__(kShortThreads, 2)
 #pragma unroll
                 for (int c = 0; c < kStageChunks; ++c)
                     blks[c] = __shfl_sync(0xffffffffu, batch_blk, (rel & 7) * kStageChunks + c);
-                const int slot = it % kShortStages;
+                const int slot = it % kStages;
                 int ok = 1;
-                if (lane == 0 && it >= kShortStages)
-                    ok = mbar_wait(&empty[slot], ((it / kShortStages) - 1) & 1, abort_flag);
+                if (lane == 0 && it >= kStages)
+                    ok = mbar_wait(&empty[slot], ((it / kStages) - 1) & 1, abort_flag);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) {
                     aborted = true;
@@ -267,8 +286,8 @@ __global__ void __launch_bounds__(kShortThreads, 2)
         if (aborted && lane == 0) {
             flag_status(p.status, PA_DEV_WAIT_TIMEOUT);
             // let copies already in flight land before the CTA exits
-            for (uint32_t k = (it > kShortStages ? it - kShortStages : 0); k < it; ++k)
-                mbar_drain(&full[k % kShortStages], (k / kShortStages) & 1);
+            for (uint32_t k = (it > kStages ? it - kStages : 0); k < it; ++k)
+                mbar_drain(&full[k % kStages], (k / kStages) & 1);
         }
         return;
     }
@@ -279,8 +298,8 @@ __global__ void __launch_bounds__(kShortThreads, 2)
     cs.active = false;
     uint32_t it = 0;
     while (true) {
-        const int slot = it % kShortStages;
-        const bool ok = warp_mbar_wait(&full[slot], (it / kShortStages) & 1, abort_flag);
+        const int slot = it % kStages;
+        const bool ok = warp_mbar_wait(&full[slot], (it / kStages) & 1, abort_flag);
         if (!ok) {
             if (lane == 0) flag_status(p.status, PA_DEV_WAIT_TIMEOUT);
             break;
@@ -296,13 +315,23 @@ __global__ void __launch_bounds__(kShortThreads, 2)
             cs.h = item_h;
             cs.split = item.split;
             cs.nsplit = item.nsplit;
-            cs.tok0 = __ldg(p.qsl + item.b);
-            const int n = __ldg(p.qsl + item.b + 1) - cs.tok0;
-            cs.ctx = __ldg(p.ctx + item.b);
+            cs.counter = item.counter * p.num_kv_heads + item_h;
+            // a piece of a request: its tokens start q_begin tokens in, so its
+            // rows' causal limits start q_begin keys further
+            cs.tok0 = __ldg(p.qsl + item.b) + item.q_begin;
+            const int n = item.q_count;
+            cs.ctx = __ldg(p.ctx + item.b) + item.q_begin;
             const int L = __ldg(p.seq_lens + item.b);
             cs.key_end = min(item.stage_end * kStageKeys, L);
             cs.R = n * p.group;
             cs.partial_base = item.partial_base + item_h * item.nsplit * cs.R;
+            if constexpr (FP8) {
+                cs.sl2 = p.scale_log2 * __ldg(p.k_scale + item_h);
+                cs.vsc = __ldg(p.v_scale + item_h);
+            } else {
+                cs.sl2 = p.scale_log2;
+                cs.vsc = 1.f;
+            }
             const int RT = (cs.R + 15) >> 4;
             const int RTp = RT >= 3 ? 4 : RT;
             cs.KQ = kShortConsumerWarps / RTp;
@@ -313,24 +342,39 @@ __global__ void __launch_bounds__(kShortThreads, 2)
             cs.limit0 = r0 < cs.R ? cs.ctx + r0 / p.group : -1;
             cs.limit1 = r1 < cs.R ? cs.ctx + r1 / p.group : -1;
             if (cs.active) {
-                const uint32_t *q0 = nullptr, *q1 = nullptr;
+                const __nv_bfloat16 *q0 = nullptr, *q1 = nullptr;
                 if (r0 < cs.R)
-                    q0 = reinterpret_cast<const uint32_t *>(
-                        p.q + (static_cast<int64_t>(cs.tok0 + r0 / p.group) * p.num_q_heads +
-                               cs.h * p.group + r0 % p.group) *
-                                  D);
+                    q0 = p.q + (static_cast<int64_t>(cs.tok0 + r0 / p.group) * p.num_q_heads +
+                                cs.h * p.group + r0 % p.group) *
+                                   D;
                 if (r1 < cs.R)
-                    q1 = reinterpret_cast<const uint32_t *>(
-                        p.q + (static_cast<int64_t>(cs.tok0 + r1 / p.group) * p.num_q_heads +
-                               cs.h * p.group + r1 % p.group) *
-                                  D);
+                    q1 = p.q + (static_cast<int64_t>(cs.tok0 + r1 / p.group) * p.num_q_heads +
+                                cs.h * p.group + r1 % p.group) *
+                                   D;
+                if constexpr (FP8) {
+                    // k-step ks, lane quad t: dims 16ks+4t .. 16ks+4t+3, as the
+                    // fp8 K fragments hold them
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int w = ks * 8 + t;  // 32-bit word index of dims ks*16 + 2t
-                    cs.qa[ks][0] = q0 ? __ldg(q0 + w) : 0u;
-                    cs.qa[ks][1] = q1 ? __ldg(q1 + w) : 0u;
-                    cs.qa[ks][2] = q0 ? __ldg(q0 + w + 4) : 0u;
-                    cs.qa[ks][3] = q1 ? __ldg(q1 + w + 4) : 0u;
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const uint2 z = make_uint2(0u, 0u);
+                        const uint2 x0 = q0 ? __ldg(reinterpret_cast<const uint2 *>(q0) + ks * 4 + t) : z;
+                        const uint2 x1 = q1 ? __ldg(reinterpret_cast<const uint2 *>(q1) + ks * 4 + t) : z;
+                        cs.qa[ks][0] = bf16x2_to_f16x2(x0.x);
+                        cs.qa[ks][1] = bf16x2_to_f16x2(x1.x);
+                        cs.qa[ks][2] = bf16x2_to_f16x2(x0.y);
+                        cs.qa[ks][3] = bf16x2_to_f16x2(x1.y);
+                    }
+                } else {
+                    const uint32_t *w0 = reinterpret_cast<const uint32_t *>(q0);
+                    const uint32_t *w1 = reinterpret_cast<const uint32_t *>(q1);
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const int w = ks * 8 + t;  // 32-bit word index of dims ks*16 + 2t
+                        cs.qa[ks][0] = w0 ? __ldg(w0 + w) : 0u;
+                        cs.qa[ks][1] = w1 ? __ldg(w1 + w) : 0u;
+                        cs.qa[ks][2] = w0 ? __ldg(w0 + w + 4) : 0u;
+                        cs.qa[ks][3] = w1 ? __ldg(w1 + w + 4) : 0u;
+                    }
                 }
             }
 #pragma unroll
@@ -354,17 +398,35 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                 for (int i = 0; i < 2; ++i)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) sacc[i][e] = 0.f;
+                if constexpr (FP8) {
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int key = (mi >> 1) * 8 + (lane & 7);
-                    const int col = (ks & 3) * 2 + (mi & 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kb + (ks >> 2) * G::kBoxBytes + sw128_offset(key, col), b0, b1, b2,
-                            b3);
-                    mma_bf16_16816(sacc[0], cs.qa[ks][0], cs.qa[ks][1], cs.qa[ks][2],
-                                   cs.qa[ks][3], b0, b1);
-                    mma_bf16_16816(sacc[1], cs.qa[ks][0], cs.qa[ks][1], cs.qa[ks][2],
-                                   cs.qa[ks][3], b2, b3);
+                    for (int ks2 = 0; ks2 < KS / 2; ++ks2) {
+                        // matrices: keys 0-7 | 8-15 of k-step 2ks2, then of 2ks2+1
+                        const int key = (mi & 1) * 8 + (lane & 7);
+                        const int col = ks2 * 2 + (mi >> 1);
+                        uint32_t r[4];
+                        ldsm_x4(kb + sw128_offset(key, col), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const int ks = ks2 * 2 + (m >> 1);
+                            mma_f16_16816(sacc[m & 1], cs.qa[ks][0], cs.qa[ks][1], cs.qa[ks][2],
+                                          cs.qa[ks][3], e4m3x2_to_f16x2(r[m] & 0xFFFFu),
+                                          e4m3x2_to_f16x2(r[m] >> 16));
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const int key = (mi >> 1) * 8 + (lane & 7);
+                        const int col = (ks & 3) * 2 + (mi & 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(kb + (ks >> 2) * G::kBoxBytes + sw128_offset(key, col), b0, b1,
+                                b2, b3);
+                        mma_bf16_16816(sacc[0], cs.qa[ks][0], cs.qa[ks][1], cs.qa[ks][2],
+                                       cs.qa[ks][3], b0, b1);
+                        mma_bf16_16816(sacc[1], cs.qa[ks][0], cs.qa[ks][1], cs.qa[ks][2],
+                                       cs.qa[ks][3], b2, b3);
+                    }
                 }
                 // scale to log2 units and mask (causal limit per row, item key range)
                 const bool need_mask = (key0 + kChunkKeys - 1 > cs.ctx) ||
@@ -373,7 +435,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        float s = sacc[nt][e] * p.scale_log2;
+                        float s = sacc[nt][e] * cs.sl2;
                         if (need_mask) {
                             const int key = key0 + nt * 8 + 2 * t + (e & 1);
                             const int lim = (e < 2) ? cs.limit0 : cs.limit1;
@@ -416,31 +478,60 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                 }
                 cs.l0 += pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
                 cs.l1 += pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
-                const uint32_t pa0 = pack_bf16x2(pr[0][0], pr[0][1]);
-                const uint32_t pa1 = pack_bf16x2(pr[0][2], pr[0][3]);
-                const uint32_t pa2 = pack_bf16x2(pr[1][0], pr[1][1]);
-                const uint32_t pa3 = pack_bf16x2(pr[1][2], pr[1][3]);
+                const uint32_t pa0 = FP8 ? pack_f16x2(pr[0][0], pr[0][1]) : pack_bf16x2(pr[0][0], pr[0][1]);
+                const uint32_t pa1 = FP8 ? pack_f16x2(pr[0][2], pr[0][3]) : pack_bf16x2(pr[0][2], pr[0][3]);
+                const uint32_t pa2 = FP8 ? pack_f16x2(pr[1][0], pr[1][1]) : pack_bf16x2(pr[1][0], pr[1][1]);
+                const uint32_t pa3 = FP8 ? pack_f16x2(pr[1][2], pr[1][3]) : pack_bf16x2(pr[1][2], pr[1][3]);
                 // V rows past the item's keys may hold anything (even NaN):
                 // zero them in the fragments of a partially valid chunk.
                 const int nvalid = cs.key_end - key0;
                 const bool tail = nvalid < kChunkKeys;
+                const bool k0 = 2 * t < nvalid, k1 = 2 * t + 1 < nvalid;
+                const bool k8 = 2 * t + 8 < nvalid, k9 = 2 * t + 9 < nvalid;
+                if constexpr (FP8) {
 #pragma unroll
-                for (int dp = 0; dp < KS; ++dp) {
-                    const int key = (mi & 1) * 8 + (lane & 7);
-                    const int col = (dp & 3) * 2 + (mi >> 1);
-                    uint32_t v0, v1, v2, v3;
-                    ldsm_x4_t(vb + (dp >> 2) * G::kBoxBytes + sw128_offset(key, col), v0, v1, v2,
-                              v3);
-                    if (tail) {
-                        const bool k0 = 2 * t < nvalid, k1 = 2 * t + 1 < nvalid;
-                        const bool k8 = 2 * t + 8 < nvalid, k9 = 2 * t + 9 < nvalid;
-                        v0 = keep_pair(v0, k0, k1);
-                        v2 = keep_pair(v2, k0, k1);
-                        v1 = keep_pair(v1, k8, k9);
-                        v3 = keep_pair(v3, k8, k9);
+                    for (int c2 = 0; c2 < D / 32; ++c2) {
+                        // matrices: keys 0-7 | 8-15 of dim group 2c2, then of 2c2+1;
+                        // lane: keys 2t, 2t+1 x dims 2j, 2j+1 (j = lane / 4)
+                        const int key = (mi & 1) * 8 + (lane & 7);
+                        const int col = c2 * 2 + (mi >> 1);
+                        uint32_t r[4];
+                        ldsm_x4_t(vb + sw128_offset(key, col), r[0], r[1], r[2], r[3]);
+                        if (tail) {
+                            r[0] = keep_pair(r[0], k0, k1);
+                            r[2] = keep_pair(r[2], k0, k1);
+                            r[1] = keep_pair(r[1], k8, k9);
+                            r[3] = keep_pair(r[3], k8, k9);
+                        }
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) r[m] = byte_perm(r[m], 0x3120u);
+                        // low halves: dim 2j (even tile), high halves: dim 2j+1 (odd tile)
+#pragma unroll
+                        for (int gsub = 0; gsub < 2; ++gsub) {
+                            const uint32_t lo = r[2 * gsub], hi = r[2 * gsub + 1];
+                            mma_f16_16816(cs.o[4 * c2 + 2 * gsub], pa0, pa1, pa2, pa3,
+                                          e4m3x2_to_f16x2(lo & 0xFFFFu), e4m3x2_to_f16x2(hi & 0xFFFFu));
+                            mma_f16_16816(cs.o[4 * c2 + 2 * gsub + 1], pa0, pa1, pa2, pa3,
+                                          e4m3x2_to_f16x2(lo >> 16), e4m3x2_to_f16x2(hi >> 16));
+                        }
                     }
-                    mma_bf16_16816(cs.o[2 * dp], pa0, pa1, pa2, pa3, v0, v1);
-                    mma_bf16_16816(cs.o[2 * dp + 1], pa0, pa1, pa2, pa3, v2, v3);
+                } else {
+#pragma unroll
+                    for (int dp = 0; dp < KS; ++dp) {
+                        const int key = (mi & 1) * 8 + (lane & 7);
+                        const int col = (dp & 3) * 2 + (mi >> 1);
+                        uint32_t v0, v1, v2, v3;
+                        ldsm_x4_t(vb + (dp >> 2) * G::kBoxBytes + sw128_offset(key, col), v0, v1,
+                                  v2, v3);
+                        if (tail) {
+                            v0 = keep_pair(v0, k0, k1);
+                            v2 = keep_pair(v2, k0, k1);
+                            v1 = keep_pair(v1, k8, k9);
+                            v3 = keep_pair(v3, k8, k9);
+                        }
+                        mma_bf16_16816(cs.o[2 * dp], pa0, pa1, pa2, pa3, v0, v1);
+                        mma_bf16_16816(cs.o[2 * dp + 1], pa0, pa1, pa2, pa3, v2, v3);
+                    }
                 }
             }
         }
@@ -450,10 +541,12 @@ __global__ void __launch_bounds__(kShortThreads, 2)
             // ---- item epilogue ----
             float l0 = quad_sum(cs.l0), l1 = quad_sum(cs.l1);
             if (cs.KQ > 1) {
-                // merge the KQ warps that share a row tile, through this stage's buffer
+                // merge the KQ warps that share a row tile, through this
+                // stage's buffer (bf16 ring) or the merge area (fp8 ring)
                 named_bar_sync(1, 32 * kShortConsumerWarps);
-                float *scratch = reinterpret_cast<float *>(stage_mem + slot * G::kStageBytes);
-                wrote_stage = true;
+                float *scratch = FP8 ? own_scratch
+                                     : reinterpret_cast<float *>(stage_mem + slot * G::kStageBytes);
+                wrote_stage = !FP8;
                 if (cs.active && cs.kq > 0) {
                     float *reg = scratch + (cs.rt * (cs.KQ - 1) + cs.kq - 1) * G::kScratchFloats;
 #pragma unroll
@@ -498,14 +591,29 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                 }
             }
             if (cs.active && cs.kq == 0) {
-                // final state of rows r0 = rt*16+g and r1 = r0+8 over this item's keys
+                // final state of rows r0 = rt*16+g and r1 = r0+8 over this item's keys.
+                // Output columns in pairs: pair pi of this lane holds dims
+                // (col, col+1) -- bf16 ring: tile pi; fp8 ring: the even and
+                // odd tiles of dim group pi/2 (see the header comment)
+                auto pair_of = [&](int pi, int half, float &x, float &y) -> int {
+                    if constexpr (FP8) {
+                        const int grp = pi >> 1, e = pi & 1;
+                        x = cs.o[2 * grp][2 * half + e];
+                        y = cs.o[2 * grp + 1][2 * half + e];
+                        return grp * 16 + 4 * t + 2 * e;
+                    } else {
+                        x = cs.o[pi][2 * half];
+                        y = cs.o[pi][2 * half + 1];
+                        return pi * 8 + 2 * t;
+                    }
+                };
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const int r = cs.rt * 16 + g + half * 8;
                     if (r >= cs.R) continue;
                     const float l = half ? l1 : l0;
                     const float m = half ? cs.m1 : cs.m0;
-                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    const float inv = l > 0.f ? cs.vsc / l : 0.f;
                     const float lse_v = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
                     const int tok = cs.tok0 + r / p.group;
                     const int hq = cs.h * p.group + r % p.group;
@@ -528,26 +636,31 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                         }
                         uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + row * D);
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            float x = cs.o[nt][half * 2] * inv, y = cs.o[nt][half * 2 + 1] * inv;
+                        for (int pi = 0; pi < NT; ++pi) {
+                            float x, y;
+                            const int col = pair_of(pi, half, x, y);
+                            x *= inv;
+                            y *= inv;
                             if (p.extra_o) {
                                 x *= wa;
                                 y *= wa;
                                 if (xo) {
-                                    const float2 e2 = __ldg(reinterpret_cast<const float2 *>(xo + nt * 8 + 2 * t));
+                                    const float2 e2 = __ldg(reinterpret_cast<const float2 *>(xo + col));
                                     x += wb * e2.x;
                                     y += wb * e2.y;
                                 }
                             }
-                            dst[(nt * 8 + 2 * t) >> 1] = pack_bf16x2(x, y);
+                            dst[col >> 1] = pack_bf16x2(x, y);
                         }
                         if (p.lse && t == 0) p.lse[row] = lse_f;
                     } else {
                         float *dst = p.partial_o + static_cast<int64_t>(cs.partial_base + r) * D;
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            __stcg(reinterpret_cast<float2 *>(dst + nt * 8 + 2 * t),
-                                   make_float2(cs.o[nt][half * 2] * inv, cs.o[nt][half * 2 + 1] * inv));
+                        for (int pi = 0; pi < NT; ++pi) {
+                            float x, y;
+                            const int col = pair_of(pi, half, x, y);
+                            __stcg(reinterpret_cast<float2 *>(dst + col), make_float2(x * inv, y * inv));
+                        }
                         if (t == 0) __stcg(p.partial_lse + cs.partial_base + r, lse_v);
                     }
                 }
@@ -560,7 +673,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                 named_bar_sync(1, 32 * kShortConsumerWarps);
                 if (threadIdx.x == 0) {
                     __threadfence();
-                    const int old = atomicAdd(p.counters + cs.b * p.num_kv_heads + cs.h, 1);
+                    const int old = atomicAdd(p.counters + cs.counter, 1);
                     const int last = (old == cs.nsplit - 1) ? 1 : 0;
                     if (last) __threadfence();
                     ctl[1] = last;
@@ -639,48 +752,51 @@ __global__ void __launch_bounds__(kShortThreads, 2)
 }
 
 size_t short_smem_bytes(int head_dim) {
-    return head_dim == 128 ? ShortGeom<128>::kSmemBytes : ShortGeom<64>::kSmemBytes;
+    return head_dim == 128 ? ShortGeom<128, false>::kSmemBytes : ShortGeom<64, false>::kSmemBytes;
 }
 
-template <int D>
+template <int D, bool FP8>
 static int configure_short() {
     static bool done = false;  // per process; attribute is per function, device-independent
     if (!done) {
-        if (cudaFuncSetAttribute(short_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 ShortGeom<D>::kSmemBytes) != cudaSuccess)
+        if (cudaFuncSetAttribute(short_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 ShortGeom<D, FP8>::kSmemBytes) != cudaSuccess)
             return PA_ERR_CUDA;
         done = true;
     }
     return PA_OK;
 }
 
-int short_max_ctas_per_sm(int head_dim) {
+template <int D, bool FP8>
+static int max_ctas() {
     int n = 0;
-    if (head_dim == 128) {
-        if (configure_short<128>() != PA_OK) return 1;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, short_kernel<128>, kShortThreads,
-                                                      ShortGeom<128>::kSmemBytes);
-    } else {
-        if (configure_short<64>() != PA_OK) return 1;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, short_kernel<64>, kShortThreads,
-                                                      ShortGeom<64>::kSmemBytes);
-    }
+    if (configure_short<D, FP8>() != PA_OK) return 1;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, short_kernel<D, FP8>, kShortThreads,
+                                                  ShortGeom<D, FP8>::kSmemBytes);
     return n > 0 ? n : 1;
 }
 
+int short_max_ctas_per_sm(int head_dim, bool fp8) {
+    if (fp8) return max_ctas<128, true>();
+    return head_dim == 128 ? max_ctas<128, false>() : max_ctas<64, false>();
+}
+
+template <int D, bool FP8>
+static int launch(const ShortParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int grid,
+                  cudaStream_t s) {
+    if (configure_short<D, FP8>() != PA_OK) return PA_ERR_CUDA;
+    PdlLaunch l(grid, kShortThreads, ShortGeom<D, FP8>::kSmemBytes, s);
+    return cudaLaunchKernelEx(&l.cfg, short_kernel<D, FP8>, p, tk, tv) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
 int launch_short(const ShortParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                 int head_dim, int grid, cudaStream_t s) {
+                 int head_dim, bool fp8, int grid, cudaStream_t s) {
     if (grid <= 0) return PA_OK;
-    if (head_dim == 128) {
-        if (configure_short<128>() != PA_OK) return PA_ERR_CUDA;
-        PdlLaunch l(grid, kShortThreads, ShortGeom<128>::kSmemBytes, s);
-        return cudaLaunchKernelEx(&l.cfg, short_kernel<128>, p, tk, tv) == cudaSuccess ? PA_OK
-                                                                                      : PA_ERR_CUDA;
-    }
-    if (configure_short<64>() != PA_OK) return PA_ERR_CUDA;
-    PdlLaunch l(grid, kShortThreads, ShortGeom<64>::kSmemBytes, s);
-    return cudaLaunchKernelEx(&l.cfg, short_kernel<64>, p, tk, tv) == cudaSuccess ? PA_OK
-                                                                                 : PA_ERR_CUDA;
+    if (fp8) return head_dim == 128 ? launch<128, true>(p, tk, tv, grid, s) : PA_ERR_UNSUPPORTED;
+    return head_dim == 128 ? launch<128, false>(p, tk, tv, grid, s)
+                           : launch<64, false>(p, tk, tv, grid, s);
 }
 
 }  // namespace pa

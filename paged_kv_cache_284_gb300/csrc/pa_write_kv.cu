@@ -1,10 +1,12 @@
 // pa_write_kv.cu -- reshape_and_cache: scatter this step's K/V rows into
-// their cache slots ("11. 推理加速(一):vLLM 原理", §11.2: tokens fill
+// their cache slots (bf16 pool: bit copy; fp8 pool: quantised per kv head) ("11. 推理加速(一):vLLM 原理", §11.2: tokens fill
 // fixed-size physical blocks; slot = block * block_size + offset).
 //
 // Pure HBM copy: each thread moves one 16-byte piece of one (token, kv head)
 // row for K and the same piece for V, so a warp covers 512 contiguous bytes
 // of the source and whole 16-byte sectors of the destination row.
+#include <cuda_fp8.h>
+
 #include "pa_internal.cuh"
 
 namespace pa {
@@ -39,9 +41,69 @@ __global__ void __launch_bounds__(256) write_kv_kernel(
     v_cache[dst] = kv_v;
 }
 
+// FP8 pool: each thread turns 16 bf16 elements of one (token, kv head) row
+// into 16 e4m3 codes, x / scale[h] in binary32 (IEEE division) then the
+// saturating round-to-nearest-even conversion, and stores them as one
+// 16-byte piece of the cache row.
+__device__ __forceinline__ uint32_t quantise4(uint2 x, float s) {
+    const float f0 = __fdiv_rn(__uint_as_float(x.x << 16), s);
+    const float f1 = __fdiv_rn(__uint_as_float(x.x & 0xFFFF0000u), s);
+    const float f2 = __fdiv_rn(__uint_as_float(x.y << 16), s);
+    const float f3 = __fdiv_rn(__uint_as_float(x.y & 0xFFFF0000u), s);
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f0, f1), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f2, f3), __NV_SATFINITE, __NV_E4M3);
+    return (lo & 0xFFFFu) | (hi << 16);
+}
+
+__global__ void __launch_bounds__(256) write_kv_fp8_kernel(
+    const uint4 *__restrict__ k, const uint4 *__restrict__ v, const int64_t *__restrict__ slots,
+    int num_tokens, int num_kv_heads, int pieces_per_row, int block_size, int num_blocks,
+    const float *__restrict__ k_scale, const float *__restrict__ v_scale,
+    uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, unsigned *status) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t per_token = static_cast<int64_t>(num_kv_heads) * pieces_per_row;
+    if (idx >= per_token * num_tokens) return;
+    const int64_t t = idx / per_token;
+    const int64_t rem = idx - t * per_token;  // = h * pieces_per_row + piece
+    const int64_t s = __ldg(slots + t);
+    if (s < 0) return;  // padding token
+    const int64_t blk = s / block_size;
+    const int64_t off = s - blk * block_size;
+    if (blk >= num_blocks) {
+        flag_status(status, PA_DEV_BAD_SLOT);
+        return;
+    }
+    const int64_t h = rem / pieces_per_row;
+    const int64_t piece = rem - h * pieces_per_row;
+    const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * pieces_per_row + piece;
+    const float ks = __ldg(k_scale + h), vs = __ldg(v_scale + h);
+    // source: 16 bf16 = two 16-byte pieces of the bf16 row
+    const uint4 ka = __ldg(k + 2 * idx), kb = __ldg(k + 2 * idx + 1);
+    const uint4 va = __ldg(v + 2 * idx), vb = __ldg(v + 2 * idx + 1);
+    k_cache[dst] = make_uint4(quantise4(make_uint2(ka.x, ka.y), ks), quantise4(make_uint2(ka.z, ka.w), ks),
+                              quantise4(make_uint2(kb.x, kb.y), ks), quantise4(make_uint2(kb.z, kb.w), ks));
+    v_cache[dst] = make_uint4(quantise4(make_uint2(va.x, va.y), vs), quantise4(make_uint2(va.z, va.w), vs),
+                              quantise4(make_uint2(vb.x, vb.y), vs), quantise4(make_uint2(vb.z, vb.w), vs));
+}
+
 int launch_write_kv(const void *k, const void *v, const int64_t *slots, int num_tokens,
                     const pa_kv_desc *kv, unsigned *status, cudaStream_t s) {
     if (num_tokens == 0) return PA_OK;
+    if (kv->kv_dtype == PA_KV_FP8_E4M3) {
+        const int pieces = kv->head_dim / 16;  // 16 codes per 16-byte piece
+        const int64_t total = static_cast<int64_t>(num_tokens) * kv->num_kv_heads * pieces;
+        const int threads = 256;
+        const int64_t blocks = (total + threads - 1) / threads;
+        PdlLaunch l(static_cast<unsigned>(blocks), threads, 0, s);
+        const cudaError_t e = cudaLaunchKernelEx(
+            &l.cfg, write_kv_fp8_kernel, static_cast<const uint4 *>(k),
+            static_cast<const uint4 *>(v), slots, num_tokens, kv->num_kv_heads, pieces,
+            kv->block_size, kv->num_blocks, kv->k_scale, kv->v_scale,
+            static_cast<uint4 *>(kv->k_cache), static_cast<uint4 *>(kv->v_cache), status);
+        return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
     const int pieces = kv->head_dim * 2 / 16;
     const int64_t total = static_cast<int64_t>(num_tokens) * kv->num_kv_heads * pieces;
     const int threads = 256;

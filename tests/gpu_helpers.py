@@ -87,3 +87,51 @@ def run_and_check(pool, steps, **kw):
         assert_attention_close(out, lse, ref_o, ref_l, f"{step.label} {kw}")
     assert_status_clean()
     return kc, vc
+
+
+# ---- FP8 (e4m3) KV pool -------------------------------------------------------
+
+def codes(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().numpy()
+
+
+def fp8_dev(pool8):
+    """Device copies of an Fp8Pool: (k codes, v codes, k_scale, v_scale)."""
+    return (pool8.k_cache.to(DEV), pool8.v_cache.to(DEV), pool8.k_scale.to(DEV),
+            pool8.v_scale.to(DEV))
+
+
+def gpu_write_fp8(step, kc, vc, ks, vs):
+    pk.pa_write_kv(step.k.to(DEV), step.v.to(DEV), step.slot_mapping.to(DEV), kc, vc,
+                   k_scale=ks, v_scale=vs)
+
+
+def gpu_attend_fp8(step, kc, vc, ks, vs, **kw):
+    q = step.q.to(DEV)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    pk.pa_attention(q, kc, vc, scale=step.scale, out=out, lse=lse, k_scale=ks, v_scale=vs,
+                    **dev_meta(step), **kw)
+    return out, lse
+
+
+def run_and_check_fp8(pool8, steps, **kw):
+    """Write + attend each step on one e4m3 pool (GPU and oracle): caches equal
+    byte for byte, attention within tolerance of the fp64 oracle over the
+    dequantised codes."""
+    kc, vc, ks, vs = fp8_dev(pool8)
+    kb, vb = codes(pool8.k_cache), codes(pool8.v_cache)
+    sk, sv = pool8.k_scale.numpy(), pool8.v_scale.numpy()
+    for step in steps:
+        gpu_write_fp8(step, kc, vc, ks, vs)
+        kb, vb = oracle.write_kv_fp8(step.k, step.v, step.slot_mapping, kb, vb, sk, sv)
+        out, lse = gpu_attend_fp8(step, kc, vc, ks, vs, **kw)
+        torch.cuda.synchronize()
+        assert np.array_equal(codes(kc), kb), f"{step.label}: fp8 K cache differs"
+        assert np.array_equal(codes(vc), vb), f"{step.label}: fp8 V cache differs"
+        ref_o, ref_l = oracle.attention_fp8(step.q, kb, vb, sk, sv, step.block_tables,
+                                            step.query_start_loc, step.context_lens,
+                                            step.seq_lens, step.scale)
+        assert_attention_close(out, lse, ref_o, ref_l, f"fp8 {step.label} {kw}")
+    assert_status_clean()
+    return kc, vc, ks, vs

@@ -101,3 +101,34 @@ def test_validate_metadata_rejects(mutate, needle):
                                 slot_mapping=m[4])
     assert e.value.code == pk.PA_ERR_BAD_METADATA
     assert needle in pk.lib().pa_last_error_message()
+
+
+def test_fp8_descriptor_is_checked_on_host():
+    """The fp8 pool's descriptor fields are validated before any CUDA call."""
+    lib = pk.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    cases = [
+        (pk.KVDesc(1 << 20, 1 << 21, 100, 16, 8, 128, 7, 0, 1 << 22, 1 << 22), pk.PA_ERR_UNSUPPORTED),
+        (pk.KVDesc(1 << 20, 1 << 21, 100, 16, 8, 64, pk.PA_KV_FP8_E4M3, 0, 1 << 22, 1 << 22),
+         pk.PA_ERR_UNSUPPORTED),                                       # fp8 needs head_dim 128
+        (pk.KVDesc(1 << 20, 1 << 21, 100, 16, 8, 128, pk.PA_KV_FP8_E4M3, 0, None, 1 << 22),
+         pk.PA_ERR_INVALID_ARG),                                       # missing k_scale
+        (pk.KVDesc(1 << 20, 1 << 21, 100, 16, 8, 128, pk.PA_KV_FP8_E4M3, 0, (1 << 22) + 2,
+                   1 << 22), pk.PA_ERR_INVALID_ARG),                   # misaligned scale
+        (pk.KVDesc(1 << 20, 1 << 21, 100, 16, 8, 128, pk.PA_KV_BF16, 3, None, None),
+         pk.PA_ERR_INVALID_ARG),                                       # reserved != 0
+    ]
+    for kv, want in cases:
+        assert lib.pa_write_kv(fake, fake, fake, 4, ctypes.byref(kv), None) == want
+    # prefix attention and cascade decode take bf16 pools only
+    kv = pk.KVDesc(1 << 20, 1 << 21, 100, 16, 8, 128, pk.PA_KV_FP8_E4M3, 0, 1 << 22, 1 << 22)
+    rc = lib.pa_prefix_attention(fake, ctypes.byref(kv), fake, 64, 4, 32, 0.1, fake, None,
+                                 ctypes.c_void_p(1 << 23), 1 << 30, None)
+    assert rc == pk.PA_ERR_UNSUPPORTED
+
+
+def test_kv_descriptor_layout():
+    """Python's ctypes mirror of pa_kv_desc: two pointers, six int32, two
+    pointers (56 bytes, pointer-aligned)."""
+    assert ctypes.sizeof(pk.KVDesc) == 56
+    assert pk.KVDesc.k_scale.offset == 40 and pk.KVDesc.v_scale.offset == 48

@@ -1,0 +1,113 @@
+"""FP8 (e4m3) KV pool on the GPU against the oracle: the quantising write is
+compared byte for byte, attention within the acceptance tolerance of the fp64
+oracle over the dequantised codes (values = code x per-kv-head scale)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_284_gb300 as pk
+from paged_kv_cache_284_gb300 import workloads
+from gpu_helpers import (DEV, assert_attention_close, assert_status_clean, codes, fp8_dev,
+                         gpu_attend_fp8, gpu_write_fp8, run_and_check_fp8)
+
+pytestmark = pytest.mark.gpu
+
+
+def test_fp8_chunked_prefill_prefix_hit_and_decode():
+    """48-token prompt in three chunks, then a 107-token prompt whose first 48
+    tokens hit the cache (59 new rows: cut into pieces of 16 tokens), with
+    decode rows in the same batch."""
+    pool, steps = workloads.chunked_prefix_decode()
+    run_and_check_fp8(workloads.fp8_pool_like(pool, 7001), steps)
+
+
+def test_fp8_decode_with_forced_splits():
+    pool, (step,) = workloads.decode_heavy(num_seqs=24, lo=40, hi=1500)
+    pool8 = workloads.fp8_pool_like(pool, 7002)
+    for split_keys in (0, 256, 1024):
+        run_and_check_fp8(pool8, [step], split_keys=split_keys)
+
+
+def test_fp8_mixed_small():
+    pool, (step,) = workloads.mixed_step(num_chunks=2, chunk_len=80, chunk_ctx=(0, 700),
+                                         num_decode=20, decode_len=(20, 1200), num_spec=6,
+                                         spec_ctx=(20, 1200))
+    run_and_check_fp8(workloads.fp8_pool_like(pool, 7003), [step])
+
+
+@pytest.mark.parametrize("block_size,hq,hkv", [(32, 8, 2), (64, 16, 2), (16, 8, 8)])
+def test_fp8_block_sizes_and_groups(block_size, hq, hkv):
+    pool, (step,) = workloads.mixed_step(num_chunks=1, chunk_len=40, chunk_ctx=(0, 300),
+                                         num_decode=10, decode_len=(20, 900), num_spec=3,
+                                         spec_ctx=(20, 900), num_q_heads=hq, num_kv_heads=hkv,
+                                         block_size=block_size)
+    run_and_check_fp8(workloads.fp8_pool_like(pool, 7004 + block_size), [step])
+
+
+def test_fp8_nan_codes_past_seq_len_are_ignored():
+    """Slots past each request's last key hold NaN codes; no output may see them."""
+    pool, (step,) = workloads.decode_heavy(num_seqs=12, lo=20, hi=400)
+    pool8 = workloads.fp8_pool_like(pool, 7010)
+    bs = step.block_size
+    for b in range(step.num_seqs):
+        L = int(step.seq_lens[b])
+        last = int(step.block_tables[b, (L - 1) // bs])
+        if L % bs:
+            pool8.k_cache[last, :, L % bs:] = 0x7F
+            pool8.v_cache[last, :, L % bs:] = 0xFF
+    run_and_check_fp8(pool8, [step])
+
+
+def test_fp8_write_quantises_out_of_range_values_by_saturation():
+    """New tokens far beyond 448 x scale saturate to +-448 (bit-exact with the
+    oracle's saturating encoder)."""
+    pool, (step,) = workloads.decode_heavy(num_seqs=6, lo=20, hi=100)
+    pool8 = workloads.fp8_pool_like(pool, 7011)
+    step.k = (step.k.float() * 300.0).to(torch.bfloat16)
+    step.v = (step.v.float() * -300.0).to(torch.bfloat16)
+    kc, vc, ks, vs = fp8_dev(pool8)
+    gpu_write_fp8(step, kc, vc, ks, vs)
+    torch.cuda.synchronize()
+    kb, vb = oracle.write_kv_fp8(step.k, step.v, step.slot_mapping, pool8.k_cache,
+                                 pool8.v_cache, pool8.k_scale, pool8.v_scale)
+    assert np.array_equal(codes(kc), kb) and np.array_equal(codes(vc), vb)
+    assert (kb == 0x7E).any() and (vb == 0xFE).any()
+    assert_status_clean()
+
+
+def test_fp8_decode_heavy_full_size_sampled():
+    """The decode-heavy step at full size on an e4m3 pool: every row finite and
+    inside the range of the values it averages; sampled requests against the
+    oracle one by one."""
+    pool, (step,) = workloads.decode_heavy()
+    pool8 = workloads.fp8_pool_like(pool, 7012)
+    del pool
+    kc, vc, ks, vs = fp8_dev(pool8)
+    gpu_write_fp8(step, kc, vc, ks, vs)
+    out, lse = gpu_attend_fp8(step, kc, vc, ks, vs)
+    torch.cuda.synchronize()
+    o = out.float()
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    vmax = float(np.abs(oracle.e4m3_decode(np.arange(256, dtype=np.uint8)[:0x7F])).max()) * \
+        float(pool8.v_scale.max())
+    assert o.abs().max().item() <= vmax * (1 + 2 ** -7)
+    kb, vb = oracle.write_kv_fp8(step.k, step.v, step.slot_mapping, pool8.k_cache,
+                                 pool8.v_cache, pool8.k_scale, pool8.v_scale)
+    idx = [0, 1, 77, 128, 200, step.num_seqs - 1]
+    sub = workloads.subset(step, idx)
+    ref_o, ref_l = oracle.attention_fp8(sub.q, kb, vb, pool8.k_scale, pool8.v_scale,
+                                        sub.block_tables, sub.query_start_loc,
+                                        sub.context_lens, sub.seq_lens, sub.scale)
+    qsl = step.query_start_loc
+    rows = torch.cat([torch.arange(int(qsl[b]), int(qsl[b + 1])) for b in idx]).to(DEV)
+    assert_attention_close(out[rows], lse[rows], ref_o, ref_l, "fp8 decode_heavy")
+    assert_status_clean()
+
+
+def test_fp8_rejected_where_not_built():
+    pool, (step,) = workloads.tiny_prefill()   # head_dim 64
+    pool8 = workloads.fp8_pool_like(pool, 7013)
+    kc, vc, ks, vs = fp8_dev(pool8)
+    with pytest.raises(pk.PaError):
+        gpu_write_fp8(step, kc, vc, ks, vs)
