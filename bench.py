@@ -129,13 +129,24 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 class DeviceStep:
-    def __init__(self, pool, step, dev, seed_note=""):
+    """One step's inputs on the device; with fp8=True the pool is an e4m3 pool
+    of the same shape (codes and per-kv-head scales drawn by the workload
+    generator) and every call passes its scales."""
+
+    def __init__(self, pool, step, dev, fp8=False):
         import paged_kv_cache_284_gb300 as pk
+        from paged_kv_cache_284_gb300 import workloads
         self.pk = pk
         self.step = step
         self.dev = dev
-        self.kc = pool.k_cache.to(dev)
-        self.vc = pool.v_cache.to(dev)
+        self.scales = {}
+        if fp8:
+            pool8 = workloads.fp8_pool_like(pool, workloads.SEED_BASE + 80)
+            self.kc, self.vc = pool8.k_cache.to(dev), pool8.v_cache.to(dev)
+            self.scales = {"k_scale": pool8.k_scale.to(dev), "v_scale": pool8.v_scale.to(dev)}
+        else:
+            self.kc = pool.k_cache.to(dev)
+            self.vc = pool.v_cache.to(dev)
         self.q = step.q.to(dev)
         self.k = step.k.to(dev)
         self.v = step.v.to(dev)
@@ -153,9 +164,9 @@ class DeviceStep:
     def run(self, write=True):
         pk = self.pk
         if write:
-            pk.pa_write_kv(self.k, self.v, self.slots, self.kc, self.vc)
+            pk.pa_write_kv(self.k, self.v, self.slots, self.kc, self.vc, **self.scales)
         pk.pa_attention(self.q, self.kc, self.vc, self.bt, self.qsl, self.ctx, self.sl,
-                        self.step.scale, self.out, self.lse, workspace=self.ws)
+                        self.step.scale, self.out, self.lse, workspace=self.ws, **self.scales)
 
 
 def split_rows(step, short_max_rows=64):
@@ -165,24 +176,25 @@ def split_rows(step, short_max_rows=64):
     return [b for b, n in enumerate(ql) if 0 < n * g <= short_max_rows]
 
 
-def algorithmic_bytes(step, reqs):
+def algorithmic_bytes(step, reqs, kv_elem_bytes=2):
     """HBM bytes a perfect kernel must move for these requests: each visible
-    K and V row once per kv head, q read once, out + lse written once, and
-    the block-table entries (per kv head)."""
+    K and V row once per kv head (kv_elem_bytes per element: 2 for bf16, 1
+    for e4m3), q read once, out + lse written once, and the block-table
+    entries (per kv head)."""
     hkv, hq, d, bs = step.num_kv_heads, step.num_q_heads, step.head_dim, step.block_size
     total = 0
     for b in reqs:
         L = int(step.seq_lens[b])
         n = int(step.query_start_loc[b + 1] - step.query_start_loc[b])
-        total += 2 * L * hkv * d * 2            # K and V
+        total += 2 * L * hkv * d * kv_elem_bytes  # K and V
         total += 2 * n * hq * d * 2 + n * hq * 4  # q, out, lse
         total += math.ceil(L / bs) * 4 * hkv     # block table
     return total
 
 
-def kv_bytes(step, reqs):
+def kv_bytes(step, reqs, kv_elem_bytes=2):
     hkv, d = step.num_kv_heads, step.head_dim
-    return sum(2 * int(step.seq_lens[b]) * hkv * d * 2 for b in reqs)
+    return sum(2 * int(step.seq_lens[b]) * hkv * d * kv_elem_bytes for b in reqs)
 
 
 def tensor_core_flops(step, reqs):
@@ -341,11 +353,13 @@ def run_ours(args):
                                              num_decode=0, num_spec=0)
     log(f"[bench] mixed step generated in {time.time() - t0:.1f}s: "
         f"{step.num_seqs} requests, {step.num_q_tokens} tokens, {pool.num_blocks} blocks")
-    ds = DeviceStep(pool, step, dev)
+    fp8 = args.kv_dtype == "fp8"
+    ds = DeviceStep(pool, step, dev, fp8=fp8)
     stream = torch.cuda.current_stream()
-    short_reqs = split_rows(step)
+    # an fp8 pool runs every row on the split-KV kernel
+    short_reqs = list(range(step.num_seqs)) if fp8 else split_rows(step)
     long_reqs = [b for b in range(step.num_seqs) if b not in set(short_reqs)]
-    short_bytes = algorithmic_bytes(step, short_reqs)
+    short_bytes = algorithmic_bytes(step, short_reqs, kv_elem_bytes=1 if fp8 else 2)
     long_flops = tensor_core_flops(step, long_reqs)
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -400,7 +414,8 @@ def run_ours(args):
     short_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[pk.PA_KERNEL_SPLIT_KV])
     long_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[pk.PA_KERNEL_TENSOR_CORE])
     achieved = short_bytes / (short_ms / 1000.0) / 1e9 if short_bytes else 0.0
-    tr = traffic_for("split_kv_mixed_step")
+    # the committed DRAM record is the bf16 variant's
+    tr = None if fp8 else traffic_for("split_kv_mixed_step")
     split_kv = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak,
                 "traffic": tr["dram_bytes_per_algorithmic_byte"] * short_bytes if tr else None,
@@ -436,9 +451,10 @@ def run_ours(args):
         def e2e_step():
             for name, t in host.items():
                 dbuf[name].copy_(t, non_blocking=True)
-            pk.pa_write_kv(dbuf["k"], dbuf["v"], dbuf["slots"], ds.kc, ds.vc)
+            pk.pa_write_kv(dbuf["k"], dbuf["v"], dbuf["slots"], ds.kc, ds.vc, **ds.scales)
             pk.pa_attention(dbuf["q"], ds.kc, ds.vc, dbuf["bt"], dbuf["qsl"], dbuf["ctx"],
-                            dbuf["sl"], step.scale, ds.out, ds.lse, workspace=ds.ws)
+                            dbuf["sl"], step.scale, ds.out, ds.lse, workspace=ds.ws,
+                            **ds.scales)
             out_h.copy_(ds.out, non_blocking=True)
             lse_h.copy_(ds.lse, non_blocking=True)
 
@@ -456,13 +472,14 @@ def run_ours(args):
     gpu_launches = 4 * args.steps   # write_kv, plan, split-KV, tensor-core per step
 
     # ---- secondary: decode-heavy KV GB/s and cascade --------------------------
-    decode = cascade = graph = None
+    decode = cascade = graph = fp8 = None
     del ds
     torch.cuda.empty_cache()
     if not args.no_secondary:
         decode = bench_decode_heavy(args, dev, hbm_peak)
         cascade = bench_cascade(args, dev)
         graph = bench_graph_decode(args, dev)
+        fp8 = bench_fp8(args, dev, hbm_peak)
 
     # ---- CPU baseline (rank 0 only) -----------------------------------------
     cpu = None
@@ -481,12 +498,16 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": "query tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 KV, f16 MMA" if fp8 else "bf16",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD if args.workload == "mixed_step" else step.label,
+            "config": {"workload": (WORKLOAD if args.workload == "mixed_step" else step.label)
+                       + ("; e4m3 KV pool, per-kv-head scales" if fp8 else ""),
+                       "kv_dtype": args.kv_dtype,
                        "requests": step.num_seqs,
                        "query_tokens": step.num_q_tokens, "pool_blocks": pool.num_blocks,
-                       "kv_bytes_read_per_step": kv_bytes(step, range(step.num_seqs)),
+                       "kv_bytes_read_per_step": kv_bytes(step, range(step.num_seqs),
+                                                          1 if fp8 else 2),
                        "l2": "inputs larger than L2 (no flush needed)",
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "seed": workloads.SEED_BASE + 3},
@@ -495,6 +516,7 @@ def run_ours(args):
             "decode_heavy": decode,
             "cascade": cascade,
             "graph_decode": graph,
+            "fp8_kv": fp8,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clocks,
@@ -578,6 +600,65 @@ def bench_graph_decode(args, dev):
     return res
 
 
+def bench_fp8(args, dev, hbm_peak):
+    """The decode-heavy and mixed steps on an e4m3 KV pool (same metadata and
+    new tokens, codes drawn by the workload generator, per-kv-head scales):
+    half the KV bytes of bf16."""
+    import paged_kv_cache_284_gb300 as pk
+    from paged_kv_cache_284_gb300 import workloads
+    res = {"kv_dtype": "e4m3 (per-kv-head fp32 scales)"}
+    for name, fn in (("decode_heavy", workloads.decode_heavy),
+                     ("mixed_step", workloads.mixed_step)):
+        pool, (step,) = fn()
+        pool8 = workloads.fp8_pool_like(pool, workloads.SEED_BASE + 80)
+        del pool
+        kc, vc = pool8.k_cache.to(dev), pool8.v_cache.to(dev)
+        ks, vs = pool8.k_scale.to(dev), pool8.v_scale.to(dev)
+        del pool8
+        q, k, v = step.q.to(dev), step.k.to(dev), step.v.to(dev)
+        slots = step.slot_mapping.to(dev)
+        meta = dict(block_tables=step.block_tables.to(dev),
+                    query_start_loc=step.query_start_loc.to(dev),
+                    context_lens=step.context_lens.to(dev), seq_lens=step.seq_lens.to(dev))
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+        T, hq, d = q.shape
+        ws = pk.alloc_workspace(pk.workspace_size(step.num_seqs, T, hq, step.num_kv_heads, d), dev)
+
+        def one(write=True):
+            if write:
+                pk.pa_write_kv(k, v, slots, kc, vc, k_scale=ks, v_scale=vs)
+            pk.pa_attention(q, kc, vc, scale=step.scale, out=out, lse=lse, workspace=ws,
+                            k_scale=ks, v_scale=vs, **meta)
+
+        for _ in range(max(3, args.warmup)):
+            one()
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        ms = time_steps(one, args.steps, stream) / args.steps
+        s_ev = make_events(args.steps)
+        it = [0]
+
+        def prof():
+            pk.set_profile_events(pk.PA_KERNEL_SPLIT_KV, *s_ev[it[0]])
+            one()
+            it[0] += 1
+
+        time_steps(prof, args.steps, stream)
+        pk.set_profile_events(pk.PA_KERNEL_SPLIT_KV, None, None)
+        k_ms = statistics.mean(a.elapsed_time(b) for a, b in s_ev)
+        reqs = range(step.num_seqs)
+        alg = algorithmic_bytes(step, reqs, kv_elem_bytes=1)
+        entry = {"step_ms": ms, "query_tokens_per_s": T / (ms / 1000),
+                 "kv_bytes": kv_bytes(step, reqs, 1), "split_kv_kernel_ms": k_ms,
+                 "split_kv_kernel_gbs": alg / (k_ms / 1000) / 1e9,
+                 "split_kv_kernel_frac": alg / (k_ms / 1000) / 1e9 / hbm_peak}
+        res[name] = entry
+        del kc, vc, ws
+        torch.cuda.empty_cache()
+    return res
+
+
 def bench_cascade(args, dev):
     import paged_kv_cache_284_gb300 as pk
     from paged_kv_cache_284_gb300 import workloads
@@ -623,6 +704,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
+                    help="KV pool element type of the headline step (fp8 = e4m3 + scales)")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--workload", choices=["mixed_step", "decode_heavy", "prefill"],

@@ -381,14 +381,14 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
     return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
-// two e4m3 codes (byte 0 -> bits 0..15, byte 1 -> bits 16..31 of the result);
-// exact: every e4m3 value is an f16 value
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-    uint32_t r;
-    asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
-        : "=r"(r)
-        : "r"(two_codes));
-    return r;
+// four e4m3 codes (bytes 0..3 of w) -> two f16x2: lo = (byte 0, byte 1),
+// hi = (byte 2, byte 3), each first code in the low half; exact, since every
+// e4m3 value is an f16 value
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 __device__ __forceinline__ uint32_t byte_perm(uint32_t x, uint32_t sel) {
     uint32_t r;

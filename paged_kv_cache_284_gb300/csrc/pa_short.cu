@@ -409,9 +409,10 @@ __global__ void __launch_bounds__(kShortThreads, 2)
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
                             const int ks = ks2 * 2 + (m >> 1);
+                            uint32_t b0, b1;
+                            e4m3x4_to_f16x2x2(r[m], b0, b1);
                             mma_f16_16816(sacc[m & 1], cs.qa[ks][0], cs.qa[ks][1], cs.qa[ks][2],
-                                          cs.qa[ks][3], e4m3x2_to_f16x2(r[m] & 0xFFFFu),
-                                          e4m3x2_to_f16x2(r[m] >> 16));
+                                          cs.qa[ks][3], b0, b1);
                         }
                     }
                 } else {
@@ -508,11 +509,12 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                         // low halves: dim 2j (even tile), high halves: dim 2j+1 (odd tile)
 #pragma unroll
                         for (int gsub = 0; gsub < 2; ++gsub) {
-                            const uint32_t lo = r[2 * gsub], hi = r[2 * gsub + 1];
-                            mma_f16_16816(cs.o[4 * c2 + 2 * gsub], pa0, pa1, pa2, pa3,
-                                          e4m3x2_to_f16x2(lo & 0xFFFFu), e4m3x2_to_f16x2(hi & 0xFFFFu));
-                            mma_f16_16816(cs.o[4 * c2 + 2 * gsub + 1], pa0, pa1, pa2, pa3,
-                                          e4m3x2_to_f16x2(lo >> 16), e4m3x2_to_f16x2(hi >> 16));
+                            // keys 0-7 (b0) and 8-15 (b1) of the even and odd tile
+                            uint32_t e0, o0, e1, o1;
+                            e4m3x4_to_f16x2x2(r[2 * gsub], e0, o0);
+                            e4m3x4_to_f16x2x2(r[2 * gsub + 1], e1, o1);
+                            mma_f16_16816(cs.o[4 * c2 + 2 * gsub], pa0, pa1, pa2, pa3, e0, e1);
+                            mma_f16_16816(cs.o[4 * c2 + 2 * gsub + 1], pa0, pa1, pa2, pa3, o0, o1);
                         }
                     }
                 } else {
