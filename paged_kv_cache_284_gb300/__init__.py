@@ -35,7 +35,12 @@ EXPORTED = ["pa_write_kv", "pa_attention_workspace_size", "pa_attention", "pa_at
             "pa_merge_states", "pa_cascade_workspace_size", "pa_prefix_attention",
             "pa_cascade_decode", "pa_validate_metadata", "pa_last_error_message",
             "pa_status_string", "pa_read_device_status", "pa_set_profile_events",
-            "pa_attention_no_alloc"]
+            "pa_attention_no_alloc",
+            # block manager (include/pa_blocks.h)
+            "pa_bm_create", "pa_bm_destroy", "pa_bm_add_request", "pa_bm_append_tokens",
+            "pa_bm_fork", "pa_bm_schedule", "pa_bm_free_request", "pa_bm_num_free_blocks",
+            "pa_bm_num_cached_blocks", "pa_bm_block_ref_count", "pa_bm_request_blocks",
+            "pa_bm_num_computed"]
 PA_KERNEL_WRITE_KV, PA_KERNEL_PLAN, PA_KERNEL_SPLIT_KV, PA_KERNEL_TENSOR_CORE = range(4)
 
 
@@ -62,6 +67,7 @@ class KVDesc(ctypes.Structure):
 
 def _declare(lib):
     P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    i64 = ctypes.c_int64
     KV = ctypes.POINTER(KVDesc)
     sig = {
         "pa_write_kv": ([P, P, P, i32, KV, P], ctypes.c_int),
@@ -83,6 +89,18 @@ def _declare(lib):
         "pa_set_profile_events": ([i32, P, P], ctypes.c_int),
         "pa_attention_no_alloc": ([P, KV, P, i32, P, P, P, i32, i32, i32, f32, P, P, P],
                                   ctypes.c_int),
+        "pa_bm_create": ([i32, i32], P),
+        "pa_bm_destroy": ([P], None),
+        "pa_bm_add_request": ([P, i64, P, i32, P], ctypes.c_int),
+        "pa_bm_append_tokens": ([P, i64, P, i32], ctypes.c_int),
+        "pa_bm_fork": ([P, i64, i64], ctypes.c_int),
+        "pa_bm_schedule": ([P, i32, P, P, i32, P, P, P, P, P, i32, P, P], ctypes.c_int),
+        "pa_bm_free_request": ([P, i64], ctypes.c_int),
+        "pa_bm_num_free_blocks": ([P], i32),
+        "pa_bm_num_cached_blocks": ([P], i32),
+        "pa_bm_block_ref_count": ([P, i32], i32),
+        "pa_bm_request_blocks": ([P, i64, P, i32], i32),
+        "pa_bm_num_computed": ([P, i64], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)

@@ -1,6 +1,7 @@
 """Build libpa.so (the C-ABI CUDA library) in-tree for sm_103a.
 
-Each .cu file under csrc/ is compiled by nvcc in parallel, then linked into
+Each source under csrc/ (.cu kernels and the host-only block manager .cpp)
+is compiled by nvcc in parallel, then linked into
 paged_kv_cache_284_gb300/libpa.so.  Objects go to _build/ (git-ignored).
 """
 from __future__ import annotations
@@ -16,7 +17,7 @@ OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpa.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 SOURCES = ["pa_api.cu", "pa_write_kv.cu", "pa_plan.cu", "pa_short.cu", "pa_long.cu",
-           "pa_merge.cu", "pa_static.cu"]
+           "pa_merge.cu", "pa_static.cu", "pa_blocks.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -44,12 +45,12 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     nvcc = _nvcc()
     os.makedirs(OBJ, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
-    headers.append(os.path.join(INCLUDE, "pa.h"))
+    headers += [os.path.join(INCLUDE, h) for h in os.listdir(INCLUDE) if h.endswith(".h")]
     jobs = []
     objs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(OBJ, src.replace(".cu", ".o"))
+        o = os.path.join(OBJ, os.path.splitext(src)[0] + ".o")
         objs.append(o)
         if force or _stale(o, [s] + headers):
             jobs.append([nvcc, "-c", s, "-o", o] + _flags(extra_flags))

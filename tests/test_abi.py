@@ -1,5 +1,5 @@
 """C-ABI checks that need no GPU: the library loads, exports every entry
-point declared in include/pa.h, rejects bad scalar arguments before touching
+point declared in include/*.h, rejects bad scalar arguments before touching
 the device, and the host-side metadata validator catches each kind of bad
 metadata."""
 import ctypes
@@ -15,9 +15,14 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def declared_functions():
-    src = open(os.path.join(ROOT, "include", "pa.h")).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", src)))
+    """Every function declared by the headers under include/."""
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for h in sorted(os.listdir(inc)):
+        if h.endswith(".h"):
+            src = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, h)).read(), flags=re.S)
+            names.update(re.findall(r"\b(pa_[a-z_]+)\s*\(", src))
+    return sorted(names)
 
 
 def test_library_exports_every_declared_function():
