@@ -30,7 +30,7 @@ def _rank(rank, world, port, results):
 def test_two_replicas_report_slowest_time_and_whole_job_throughput():
     world = 2
     port = 29500 + (os.getpid() % 2000)
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.spawn(_rank, args=(world, port, results), nprocs=world, join=True)
         res = dict(results)
