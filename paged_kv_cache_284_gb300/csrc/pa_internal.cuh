@@ -390,6 +390,12 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint
         : "=r"(lo), "=r"(hi)
         : "r"(w));
 }
+// transpose of an 8x8 b16 matrix held as one mma fragment register per lane
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
 __device__ __forceinline__ uint32_t byte_perm(uint32_t x, uint32_t sel) {
     uint32_t r;
     asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(x), "r"(sel));

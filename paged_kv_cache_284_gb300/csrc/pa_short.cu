@@ -6,10 +6,11 @@
 //
 // Design (one persistent CTA per SM slot, 5 warps):
 //  * warp 4 is the producer: it pulls work items (request b, kv head h, key
-//    range) from a device counter, reads the block table 32 chunks at a time
-//    and issues TMA tensor loads (128-byte swizzled boxes of 16 keys x 64
-//    dims) of K and V into a 3-deep ring of 64-key stages.  The ring keeps
-//    running across item boundaries.
+//    range) from a device counter, turns the block table into TMA row
+//    coordinates 32 chunks at a time (one lane per chunk), and four lanes
+//    issue the TMA tensor loads (128-byte swizzled boxes of 16 keys x 64
+//    dims) of a stage's four chunks of K and V at once, into a 3-deep ring
+//    of 64-key stages.  The ring keeps running across item boundaries.
 //  * warps 0-3 consume: for each 16-key chunk, S = Q K^T and O += P V on
 //    mma.sync (bf16 in, fp32 accumulate) with an online softmax in the
 //    log2 domain.  All g query heads of a kv head (and all q_len rows) are
@@ -32,6 +33,13 @@
 //    dims of a pair land in two different 8-column output tiles; the output
 //    columns are permuted back when they are written.  Scores are scaled by
 //    the kv head's K scale, outputs by its V scale.
+//  * fp8 items with at most 8 rows (decode at group <= 8) swap the operands:
+//    S^T = K Q^T puts the chunk's 16 keys on the MMA's M side and the rows on
+//    N = 8, and O^T = V^T P^T puts 16 head dims on M, so a chunk takes 16
+//    MMAs instead of 32 and each lane holds 2 keys x 2 rows.  P^T reaches
+//    the second MMA's B operand through movmatrix (8x8 transposes).  The
+//    row maximum is reduced across lanes only when some score exceeds the
+//    running maximum by more than 2^8 (the lazy rescale threshold).
 #include "pa_internal.cuh"
 
 namespace pa {
@@ -86,6 +94,7 @@ struct Consumer {
     // item-wide
     int b, h, tok0, ctx, key_end, R, KQ, rt, kq, nsplit, split, partial_base, counter;
     float sl2, vsc;  // score scale (log2 units) and value scale
+    bool swapped;    // fp8 pool, R <= 8: S^T = K Q^T and O^T = V^T P^T
     bool active;
     // per thread: rows g and g+8 of this warp's 16-row tile
     int limit0, limit1;
@@ -94,11 +103,12 @@ struct Consumer {
     float m0, m1, l0, l1;
 };
 
-// Block id of chunk first_stage*4 + lane of a split-KV item (one lane per
-// chunk of an 8-stage batch), or -1 past the item's keys.  Out-of-range
-// table columns and block ids are clamped and flagged.
-__device__ __forceinline__ int block_id_of(const ShortParams &p, const ShortItem &item, int L,
-                                           int first_stage, int lane) {
+// TMA row coordinate (cache row = (block, kv head h, offset)) of chunk
+// first_stage*4 + lane of a split-KV item -- one lane per chunk of an
+// 8-stage batch -- or -1 past the item's keys.  Out-of-range table columns
+// and block ids are clamped and flagged.
+__device__ __forceinline__ int chunk_row_of(const ShortParams &p, const ShortItem &item, int h,
+                                            int L, int first_stage, int lane) {
     const int key_end = min(item.stage_end * kStageKeys, L);
     const int key0 = (first_stage * kStageChunks + lane) * kChunkKeys;
     if (key0 >= key_end) return -1;
@@ -112,7 +122,7 @@ __device__ __forceinline__ int block_id_of(const ShortParams &p, const ShortItem
         flag_status(p.status, PA_DEV_BAD_BLOCK);
         blk = min(max(blk, 0), p.num_blocks - 1);
     }
-    return blk;
+    return (blk * p.num_kv_heads + h) * p.block_size + key0 % p.block_size;
 }
 
 // Work item idx: its record and kv head.
@@ -120,6 +130,202 @@ __device__ __forceinline__ ShortItem short_work(const ShortParams &p, int idx, i
     const int rec = idx / p.num_kv_heads;
     h = idx - rec * p.num_kv_heads;
     return load_record(p.items, rec);
+}
+
+// One 16-key chunk of an fp8 item with at most 8 rows, operands swapped.
+// Lane (g = lane/4, t = lane%4) holds scores of keys g, g+8 for rows 2t,
+// 2t+1, and O^T tile cc's elements (dim 16cc+2g | 16cc+2g+1) x (row 2t |
+// 2t+1): cs.o[cc][0] = (row 2t, dim 16cc+2g), [1] = (2t+1, 16cc+2g),
+// [2] = (2t, 16cc+2g+1), [3] = (2t+1, 16cc+2g+1).
+template <int D>
+__device__ __forceinline__ void swapped_chunk(Consumer<D> &cs, uint32_t kb, uint32_t vb, int key0,
+                                              int lane) {
+    constexpr int KS = D / 16;
+    const int g = lane >> 2, t = lane & 3, mi = lane >> 3;
+    // S^T = K Q^T, two accumulators (even / odd k-steps) for shorter chains
+    float st[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st[h][e] = 0.f;
+#pragma unroll
+    for (int ks2 = 0; ks2 < KS / 2; ++ks2) {
+        // matrices: keys 0-7 | 8-15 of k-step 2ks2, then of 2ks2+1
+        const int key = (mi & 1) * 8 + (lane & 7);
+        const int col = ks2 * 2 + (mi >> 1);
+        uint32_t r[4];
+        ldsm_x4(kb + sw128_offset(key, col), r[0], r[1], r[2], r[3]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t a0, a1, a2, a3;
+            e4m3x4_to_f16x2x2(r[2 * h], a0, a2);      // key g:   dims 4t,4t+1 | 4t+2,4t+3
+            e4m3x4_to_f16x2x2(r[2 * h + 1], a1, a3);  // key g+8
+            const int ks = ks2 * 2 + h;
+            mma_f16_16816(st[h], a0, a1, a2, a3, cs.qa[ks][0], cs.qa[ks][1]);
+        }
+    }
+    float s[4];
+    const bool need_mask = (key0 + kChunkKeys - 1 > cs.ctx) || (key0 + kChunkKeys > cs.key_end);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        s[e] = (st[0][e] + st[1][e]) * cs.sl2;
+        if (need_mask) {
+            const int key = key0 + g + (e >> 1) * 8;
+            const int lim = (e & 1) ? cs.limit1 : cs.limit0;
+            if (key > lim || key >= cs.key_end) s[e] = -INFINITY;
+        }
+    }
+    // lazy max: reduce over the 8 lanes of a row only when needed
+    const float la = fmaxf(s[0], s[2]), lb = fmaxf(s[1], s[3]);
+    const bool ua = la > cs.m0 + kRescaleThreshold || (cs.m0 == -INFINITY && la > -INFINITY);
+    const bool ub = lb > cs.m1 + kRescaleThreshold || (cs.m1 == -INFINITY && lb > -INFINITY);
+    if (__any_sync(0xffffffffu, ua || ub)) {
+        float ma = la, mb = lb;
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, o));
+            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+        }
+        const bool up0 = ma > cs.m0 + kRescaleThreshold || (cs.m0 == -INFINITY && ma > -INFINITY);
+        const bool up1 = mb > cs.m1 + kRescaleThreshold || (cs.m1 == -INFINITY && mb > -INFINITY);
+        const float a0 = up0 ? (cs.m0 == -INFINITY ? 0.f : exp2f(cs.m0 - ma)) : 1.f;
+        const float a1 = up1 ? (cs.m1 == -INFINITY ? 0.f : exp2f(cs.m1 - mb)) : 1.f;
+        if (up0) cs.m0 = ma;
+        if (up1) cs.m1 = mb;
+        cs.l0 *= a0;
+        cs.l1 *= a1;
+#pragma unroll
+        for (int cc = 0; cc < D / 16; ++cc) {
+            cs.o[cc][0] *= a0;
+            cs.o[cc][2] *= a0;
+            cs.o[cc][1] *= a1;
+            cs.o[cc][3] *= a1;
+        }
+    }
+    const float ref0 = cs.m0 == -INFINITY ? 0.f : cs.m0;
+    const float ref1 = cs.m1 == -INFINITY ? 0.f : cs.m1;
+    const float p0 = exp2f(s[0] - ref0), p1 = exp2f(s[1] - ref1);
+    const float p2 = exp2f(s[2] - ref0), p3 = exp2f(s[3] - ref1);
+    cs.l0 += p0 + p2;
+    cs.l1 += p1 + p3;
+    // P^T fragments (key g | g+8) x (rows 2t, 2t+1) -> P fragments of row g
+    const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
+    const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
+    // O^T += V^T P^T; V rows past the item's keys are zeroed in the fragments
+    const int nvalid = cs.key_end - key0;
+    const bool tail = nvalid < kChunkKeys;
+    const bool k0 = 2 * t < nvalid, k1 = 2 * t + 1 < nvalid;
+    const bool k8 = 2 * t + 8 < nvalid, k9 = 2 * t + 9 < nvalid;
+#pragma unroll
+    for (int c2 = 0; c2 < D / 32; ++c2) {
+        // matrices: keys 0-7 | 8-15 of dim group 2c2, then of 2c2+1; lane:
+        // keys 2t, 2t+1 x dims 2g, 2g+1 of the group
+        const int key = (mi & 1) * 8 + (lane & 7);
+        const int col = c2 * 2 + (mi >> 1);
+        uint32_t r[4];
+        ldsm_x4_t(vb + sw128_offset(key, col), r[0], r[1], r[2], r[3]);
+        if (tail) {
+            r[0] = keep_pair(r[0], k0, k1);
+            r[2] = keep_pair(r[2], k0, k1);
+            r[1] = keep_pair(r[1], k8, k9);
+            r[3] = keep_pair(r[3], k8, k9);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t a0, a1, a2, a3;
+            // low halves: dim 16cc+2g (A row g), high: 16cc+2g+1 (A row g+8)
+            e4m3x4_to_f16x2x2(byte_perm(r[2 * h], 0x3120u), a0, a1);
+            e4m3x4_to_f16x2x2(byte_perm(r[2 * h + 1], 0x3120u), a2, a3);
+            mma_f16_16816(cs.o[2 * c2 + h], a0, a1, a2, a3, pb0, pb1);
+        }
+    }
+}
+
+// Item epilogue of a swapped fp8 item: row sums over the 8 lanes of a row,
+// the 4 consumer warps merged through the merge area, then warp 0 writes
+// rows 2t and 2t+1 (output or partial state).  A cascade prefix state is
+// never folded here: cascade calls take bf16 pools only.
+template <int D>
+__device__ __forceinline__ void swapped_epilogue(Consumer<D> &cs, const ShortParams &p,
+                                                 float *scratch, int lane, int warp) {
+    constexpr int kRowsFloats = 8 * D;      // floats of one warp's 8 x D block
+    constexpr int kSlot = kRowsFloats + 16;  // + 8 maxima + 8 sums
+    const int g = lane >> 2, t = lane & 3;
+    float la = cs.l0, lb = cs.l1;
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        la += __shfl_xor_sync(0xffffffffu, la, o);
+        lb += __shfl_xor_sync(0xffffffffu, lb, o);
+    }
+    named_bar_sync(1, 32 * kShortConsumerWarps);
+    if (cs.kq > 0) {
+        float *reg = scratch + (cs.kq - 1) * kSlot;
+#pragma unroll
+        for (int cc = 0; cc < D / 16; ++cc) {
+            *reinterpret_cast<float2 *>(reg + (2 * t) * D + cc * 16 + 2 * g) =
+                make_float2(cs.o[cc][0], cs.o[cc][2]);
+            *reinterpret_cast<float2 *>(reg + (2 * t + 1) * D + cc * 16 + 2 * g) =
+                make_float2(cs.o[cc][1], cs.o[cc][3]);
+        }
+        if (g == 0) {
+            reg[kRowsFloats + 2 * t] = cs.m0;
+            reg[kRowsFloats + 2 * t + 1] = cs.m1;
+            reg[kRowsFloats + 8 + 2 * t] = la;
+            reg[kRowsFloats + 8 + 2 * t + 1] = lb;
+        }
+    }
+    named_bar_sync(1, 32 * kShortConsumerWarps);
+    if (cs.kq != 0) return;
+    for (int k = 1; k < cs.KQ; ++k) {
+        const float *reg = scratch + (k - 1) * kSlot;
+        const float om0 = reg[kRowsFloats + 2 * t], om1 = reg[kRowsFloats + 2 * t + 1];
+        const float ol0 = reg[kRowsFloats + 8 + 2 * t], ol1 = reg[kRowsFloats + 8 + 2 * t + 1];
+        const float M0 = fmaxf(cs.m0, om0), M1 = fmaxf(cs.m1, om1);
+        const float a0 = cs.m0 == -INFINITY ? 0.f : exp2f(cs.m0 - M0);
+        const float b0 = om0 == -INFINITY ? 0.f : exp2f(om0 - M0);
+        const float a1 = cs.m1 == -INFINITY ? 0.f : exp2f(cs.m1 - M1);
+        const float b1 = om1 == -INFINITY ? 0.f : exp2f(om1 - M1);
+        la = a0 * la + b0 * ol0;
+        lb = a1 * lb + b1 * ol1;
+        cs.m0 = M0;
+        cs.m1 = M1;
+#pragma unroll
+        for (int cc = 0; cc < D / 16; ++cc) {
+            const float2 x = *reinterpret_cast<const float2 *>(reg + (2 * t) * D + cc * 16 + 2 * g);
+            const float2 y = *reinterpret_cast<const float2 *>(reg + (2 * t + 1) * D + cc * 16 + 2 * g);
+            cs.o[cc][0] = a0 * cs.o[cc][0] + b0 * x.x;
+            cs.o[cc][2] = a0 * cs.o[cc][2] + b0 * x.y;
+            cs.o[cc][1] = a1 * cs.o[cc][1] + b1 * y.x;
+            cs.o[cc][3] = a1 * cs.o[cc][3] + b1 * y.y;
+        }
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int r = 2 * t + half;
+        if (r >= cs.R) continue;
+        const float l = half ? lb : la;
+        const float m = half ? cs.m1 : cs.m0;
+        const float inv = l > 0.f ? cs.vsc / l : 0.f;
+        const float lse_v = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+        const int tok = cs.tok0 + r / p.group;
+        const int hq = cs.h * p.group + r % p.group;
+        const int64_t row = static_cast<int64_t>(tok) * p.num_q_heads + hq;
+        if (cs.nsplit == 1) {
+            uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + row * D);
+#pragma unroll
+            for (int cc = 0; cc < D / 16; ++cc)
+                dst[(cc * 16 + 2 * g) >> 1] =
+                    pack_bf16x2(cs.o[cc][half] * inv, cs.o[cc][2 + half] * inv);
+            if (p.lse && g == 0) p.lse[row] = lse_v;
+        } else {
+            float *dst = p.partial_o + static_cast<int64_t>(cs.partial_base + r) * D;
+#pragma unroll
+            for (int cc = 0; cc < D / 16; ++cc)
+                __stcg(reinterpret_cast<float2 *>(dst + cc * 16 + 2 * g),
+                       make_float2(cs.o[cc][half] * inv, cs.o[cc][2 + half] * inv));
+            if (g == 0) __stcg(p.partial_lse + cs.partial_base + r, lse_v);
+        }
+    }
 }
 
 }  // namespace
@@ -184,11 +390,11 @@ __global__ void __launch_bounds__(kShortThreads, 2)
         if (lane == 0) cur_idx = atomicAdd(&p.hdr->short_next, 1);
         cur_idx = __shfl_sync(0xffffffffu, cur_idx, 0);
         ShortItem cur{};
-        int cur_h = 0, cur_L = 0, cur_blk = -1;
+        int cur_h = 0, cur_L = 0, cur_row = -1;
         if (cur_idx < num_items) {
             cur = short_work(p, cur_idx, cur_h);
             cur_L = __ldg(p.seq_lens + cur.b);
-            cur_blk = block_id_of(p, cur, cur_L, cur.stage_begin, lane);
+            cur_row = chunk_row_of(p, cur, cur_h, cur_L, cur.stage_begin, lane);
         }
         while (!aborted) {
             if (cur_idx >= num_items) {
@@ -208,19 +414,20 @@ __global__ void __launch_bounds__(kShortThreads, 2)
             int nxt_idx = 0;
             if (lane == 0) nxt_idx = atomicAdd(&p.hdr->short_next, 1);  // read two stages later
             ShortItem nxt{};
-            int nxt_h = 0, nxt_L = 0, nxt_blk = -1, pf = 0;  // prefetch state of the next item
+            int nxt_h = 0, nxt_L = 0, nxt_row = -1, pf = 0;  // prefetch state of the next item
             const int nst = cur.stage_end - cur.stage_begin;
-            int batch_blk = cur_blk, next_batch = -1;
+            int batch_row = cur_row, next_batch = -1;
             for (int rel = 0; rel < nst; ++rel, ++it) {
                 const int st = cur.stage_begin + rel;
                 if ((rel & 7) == 0) {
-                    if (rel > 0) batch_blk = next_batch;
-                    next_batch = (rel + 8 < nst) ? block_id_of(p, cur, cur_L, st + 8, lane) : -1;
+                    if (rel > 0) batch_row = next_batch;
+                    next_batch =
+                        (rel + 8 < nst) ? chunk_row_of(p, cur, cur_h, cur_L, st + 8, lane) : -1;
                 }
-                int blks[kStageChunks];
-#pragma unroll
-                for (int c = 0; c < kStageChunks; ++c)
-                    blks[c] = __shfl_sync(0xffffffffu, batch_blk, (rel & 7) * kStageChunks + c);
+                // lane c < 4 takes the row of chunk c of this stage
+                const int crow =
+                    __shfl_sync(0xffffffffu, batch_row, (rel & 7) * kStageChunks + (lane & 3));
+                const int nvalid = __popc(__ballot_sync(0xffffffffu, lane < kStageChunks && crow >= 0));
                 const int slot = it % kStages;
                 int ok = 1;
                 if (lane == 0 && it >= kStages)
@@ -231,9 +438,6 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                     break;
                 }
                 if (lane == 0) {
-                    int nvalid = 0;
-#pragma unroll
-                    for (int c = 0; c < kStageChunks; ++c) nvalid += blks[c] >= 0;
                     StageMeta mm;
                     mm.item = cur_idx;
                     mm.stage = st;
@@ -242,17 +446,14 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                     meta[slot] = mm;
                     mbar_arrive_expect_tx(&full[slot],
                                           static_cast<uint32_t>(nvalid * 2 * G::kChunkBytes));
+                }
+                __syncwarp();
+                // the four chunks' copies are issued by four lanes at once
+                if (lane < kStageChunks && crow >= 0) {
 #pragma unroll
-                    for (int c = 0; c < kStageChunks; ++c) {
-                        if (blks[c] < 0) continue;
-                        const int key0 = (st * kStageChunks + c) * kChunkKeys;
-                        const int row = (blks[c] * p.num_kv_heads + cur_h) * p.block_size +
-                                        key0 % p.block_size;
-#pragma unroll
-                        for (int hf = 0; hf < G::kHalves; ++hf) {
-                            tma_load_2d(k_box(slot, c, hf), &tmk, hf * 64, row, &full[slot]);
-                            tma_load_2d(v_box(slot, c, hf), &tmv, hf * 64, row, &full[slot]);
-                        }
+                    for (int hf = 0; hf < G::kHalves; ++hf) {
+                        tma_load_2d(k_box(slot, lane, hf), &tmk, hf * 64, crow, &full[slot]);
+                        tma_load_2d(v_box(slot, lane, hf), &tmv, hf * 64, crow, &full[slot]);
                     }
                 }
                 __syncwarp();
@@ -268,7 +469,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                         pf = 2;
                     } else if (pf == 2 && (rel >= 4 || rel == nst - 1)) {
                         if (nxt_idx < num_items)
-                            nxt_blk = block_id_of(p, nxt, nxt_L, nxt.stage_begin, lane);
+                            nxt_row = chunk_row_of(p, nxt, nxt_h, nxt_L, nxt.stage_begin, lane);
                         pf = 3;
                     } else {
                         break;
@@ -281,7 +482,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
             cur = nxt;
             cur_h = nxt_h;
             cur_L = nxt_L;
-            cur_blk = nxt_blk;
+            cur_row = nxt_row;
         }
         if (aborted && lane == 0) {
             flag_status(p.status, PA_DEV_WAIT_TIMEOUT);
@@ -338,10 +539,30 @@ __global__ void __launch_bounds__(kShortThreads, 2)
             cs.rt = warp / cs.KQ;
             cs.kq = warp % cs.KQ;
             cs.active = cs.rt < RT;
+            cs.swapped = FP8 && cs.R <= 8;
             const int r0 = cs.rt * 16 + g, r1 = r0 + 8;
             cs.limit0 = r0 < cs.R ? cs.ctx + r0 / p.group : -1;
             cs.limit1 = r1 < cs.R ? cs.ctx + r1 / p.group : -1;
-            if (cs.active) {
+            if (FP8 && cs.swapped) {
+                // lane: rows 2t and 2t+1 of the scores, q row g of Q^T; Q^T
+                // fragment of k-step ks = q row g, dims 16ks+4t .. +3 (the
+                // same dim permutation as the K fragments)
+                const int ra = 2 * t, rb = 2 * t + 1;
+                cs.limit0 = ra < cs.R ? cs.ctx + ra / p.group : -1;
+                cs.limit1 = rb < cs.R ? cs.ctx + rb / p.group : -1;
+                const __nv_bfloat16 *qg = nullptr;
+                if (g < cs.R)
+                    qg = p.q + (static_cast<int64_t>(cs.tok0 + g / p.group) * p.num_q_heads +
+                                cs.h * p.group + g % p.group) *
+                                   D;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const uint2 x = qg ? __ldg(reinterpret_cast<const uint2 *>(qg) + ks * 4 + t)
+                                       : make_uint2(0u, 0u);
+                    cs.qa[ks][0] = bf16x2_to_f16x2(x.x);
+                    cs.qa[ks][1] = bf16x2_to_f16x2(x.y);
+                }
+            } else if (cs.active) {
                 const __nv_bfloat16 *q0 = nullptr, *q1 = nullptr;
                 if (r0 < cs.R)
                     q0 = p.q + (static_cast<int64_t>(cs.tok0 + r0 / p.group) * p.num_q_heads +
@@ -393,6 +614,12 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                 const uint32_t kb = smem_u32(k_box(slot, c, 0));
                 const uint32_t vb = smem_u32(v_box(slot, c, 0));
                 const int mi = lane >> 3;
+                if constexpr (FP8) {
+                    if (cs.swapped) {
+                        swapped_chunk<D>(cs, kb, vb, key0, lane);
+                        continue;
+                    }
+                }
                 float sacc[2][4];
 #pragma unroll
                 for (int i = 0; i < 2; ++i)
@@ -541,129 +768,133 @@ __global__ void __launch_bounds__(kShortThreads, 2)
         bool wrote_stage = false;
         if (mm.flags & kLast) {
             // ---- item epilogue ----
-            float l0 = quad_sum(cs.l0), l1 = quad_sum(cs.l1);
-            if (cs.KQ > 1) {
-                // merge the KQ warps that share a row tile, through this
-                // stage's buffer (bf16 ring) or the merge area (fp8 ring)
-                named_bar_sync(1, 32 * kShortConsumerWarps);
-                float *scratch = FP8 ? own_scratch
-                                     : reinterpret_cast<float *>(stage_mem + slot * G::kStageBytes);
-                wrote_stage = !FP8;
-                if (cs.active && cs.kq > 0) {
-                    float *reg = scratch + (cs.rt * (cs.KQ - 1) + cs.kq - 1) * G::kScratchFloats;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        *reinterpret_cast<float2 *>(reg + g * D + nt * 8 + 2 * t) =
-                            make_float2(cs.o[nt][0], cs.o[nt][1]);
-                        *reinterpret_cast<float2 *>(reg + (g + 8) * D + nt * 8 + 2 * t) =
-                            make_float2(cs.o[nt][2], cs.o[nt][3]);
-                    }
-                    if (t == 0) {
-                        reg[16 * D + g] = cs.m0;
-                        reg[16 * D + g + 8] = cs.m1;
-                        reg[16 * D + 16 + g] = l0;
-                        reg[16 * D + 16 + g + 8] = l1;
-                    }
-                }
-                named_bar_sync(1, 32 * kShortConsumerWarps);
-                if (cs.active && cs.kq == 0) {
-                    for (int k = 1; k < cs.KQ; ++k) {
-                        const float *reg = scratch + (cs.rt * (cs.KQ - 1) + k - 1) * G::kScratchFloats;
-                        const float om0 = reg[16 * D + g], om1 = reg[16 * D + g + 8];
-                        const float ol0 = reg[16 * D + 16 + g], ol1 = reg[16 * D + 16 + g + 8];
-                        const float M0 = fmaxf(cs.m0, om0), M1 = fmaxf(cs.m1, om1);
-                        const float a0 = cs.m0 == -INFINITY ? 0.f : exp2f(cs.m0 - M0);
-                        const float b0 = om0 == -INFINITY ? 0.f : exp2f(om0 - M0);
-                        const float a1 = cs.m1 == -INFINITY ? 0.f : exp2f(cs.m1 - M1);
-                        const float b1 = om1 == -INFINITY ? 0.f : exp2f(om1 - M1);
-                        l0 = a0 * l0 + b0 * ol0;
-                        l1 = a1 * l1 + b1 * ol1;
-                        cs.m0 = M0;
-                        cs.m1 = M1;
-#pragma unroll
+            if (FP8 && cs.swapped) {
+                swapped_epilogue<D>(cs, p, own_scratch, lane, warp);
+            } else {
+                float l0 = quad_sum(cs.l0), l1 = quad_sum(cs.l1);
+                if (cs.KQ > 1) {
+                    // merge the KQ warps that share a row tile, through this
+                    // stage's buffer (bf16 ring) or the merge area (fp8 ring)
+                    named_bar_sync(1, 32 * kShortConsumerWarps);
+                    float *scratch = FP8 ? own_scratch
+                                         : reinterpret_cast<float *>(stage_mem + slot * G::kStageBytes);
+                    wrote_stage = !FP8;
+                    if (cs.active && cs.kq > 0) {
+                        float *reg = scratch + (cs.rt * (cs.KQ - 1) + cs.kq - 1) * G::kScratchFloats;
+    #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            const float2 x = *reinterpret_cast<const float2 *>(reg + g * D + nt * 8 + 2 * t);
-                            const float2 y = *reinterpret_cast<const float2 *>(reg + (g + 8) * D + nt * 8 + 2 * t);
-                            cs.o[nt][0] = a0 * cs.o[nt][0] + b0 * x.x;
-                            cs.o[nt][1] = a0 * cs.o[nt][1] + b0 * x.y;
-                            cs.o[nt][2] = a1 * cs.o[nt][2] + b1 * y.x;
-                            cs.o[nt][3] = a1 * cs.o[nt][3] + b1 * y.y;
+                            *reinterpret_cast<float2 *>(reg + g * D + nt * 8 + 2 * t) =
+                                make_float2(cs.o[nt][0], cs.o[nt][1]);
+                            *reinterpret_cast<float2 *>(reg + (g + 8) * D + nt * 8 + 2 * t) =
+                                make_float2(cs.o[nt][2], cs.o[nt][3]);
+                        }
+                        if (t == 0) {
+                            reg[16 * D + g] = cs.m0;
+                            reg[16 * D + g + 8] = cs.m1;
+                            reg[16 * D + 16 + g] = l0;
+                            reg[16 * D + 16 + g + 8] = l1;
                         }
                     }
-                }
-            }
-            if (cs.active && cs.kq == 0) {
-                // final state of rows r0 = rt*16+g and r1 = r0+8 over this item's keys.
-                // Output columns in pairs: pair pi of this lane holds dims
-                // (col, col+1) -- bf16 ring: tile pi; fp8 ring: the even and
-                // odd tiles of dim group pi/2 (see the header comment)
-                auto pair_of = [&](int pi, int half, float &x, float &y) -> int {
-                    if constexpr (FP8) {
-                        const int grp = pi >> 1, e = pi & 1;
-                        x = cs.o[2 * grp][2 * half + e];
-                        y = cs.o[2 * grp + 1][2 * half + e];
-                        return grp * 16 + 4 * t + 2 * e;
-                    } else {
-                        x = cs.o[pi][2 * half];
-                        y = cs.o[pi][2 * half + 1];
-                        return pi * 8 + 2 * t;
-                    }
-                };
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int r = cs.rt * 16 + g + half * 8;
-                    if (r >= cs.R) continue;
-                    const float l = half ? l1 : l0;
-                    const float m = half ? cs.m1 : cs.m0;
-                    const float inv = l > 0.f ? cs.vsc / l : 0.f;
-                    const float lse_v = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
-                    const int tok = cs.tok0 + r / p.group;
-                    const int hq = cs.h * p.group + r % p.group;
-                    const int64_t row = static_cast<int64_t>(tok) * p.num_q_heads + hq;
-                    if (cs.nsplit == 1) {
-                        float wa = 1.f, wb = 0.f, lse_f = lse_v;
-                        const float *xo = nullptr;
-                        if (p.extra_o) {
-                            const float xl = __ldg(p.extra_lse + row);
-                            const float M = fmaxf(lse_v, xl);
-                            if (M == -INFINITY) {
-                                wa = 0.f;
-                            } else {
-                                const float ea = __expf(lse_v - M), eb = __expf(xl - M);
-                                wa = ea / (ea + eb);
-                                wb = eb / (ea + eb);
-                                lse_f = M + __logf(ea + eb);
-                                xo = p.extra_o + row * D;
+                    named_bar_sync(1, 32 * kShortConsumerWarps);
+                    if (cs.active && cs.kq == 0) {
+                        for (int k = 1; k < cs.KQ; ++k) {
+                            const float *reg = scratch + (cs.rt * (cs.KQ - 1) + k - 1) * G::kScratchFloats;
+                            const float om0 = reg[16 * D + g], om1 = reg[16 * D + g + 8];
+                            const float ol0 = reg[16 * D + 16 + g], ol1 = reg[16 * D + 16 + g + 8];
+                            const float M0 = fmaxf(cs.m0, om0), M1 = fmaxf(cs.m1, om1);
+                            const float a0 = cs.m0 == -INFINITY ? 0.f : exp2f(cs.m0 - M0);
+                            const float b0 = om0 == -INFINITY ? 0.f : exp2f(om0 - M0);
+                            const float a1 = cs.m1 == -INFINITY ? 0.f : exp2f(cs.m1 - M1);
+                            const float b1 = om1 == -INFINITY ? 0.f : exp2f(om1 - M1);
+                            l0 = a0 * l0 + b0 * ol0;
+                            l1 = a1 * l1 + b1 * ol1;
+                            cs.m0 = M0;
+                            cs.m1 = M1;
+    #pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                const float2 x = *reinterpret_cast<const float2 *>(reg + g * D + nt * 8 + 2 * t);
+                                const float2 y = *reinterpret_cast<const float2 *>(reg + (g + 8) * D + nt * 8 + 2 * t);
+                                cs.o[nt][0] = a0 * cs.o[nt][0] + b0 * x.x;
+                                cs.o[nt][1] = a0 * cs.o[nt][1] + b0 * x.y;
+                                cs.o[nt][2] = a1 * cs.o[nt][2] + b1 * y.x;
+                                cs.o[nt][3] = a1 * cs.o[nt][3] + b1 * y.y;
                             }
                         }
-                        uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + row * D);
-#pragma unroll
-                        for (int pi = 0; pi < NT; ++pi) {
-                            float x, y;
-                            const int col = pair_of(pi, half, x, y);
-                            x *= inv;
-                            y *= inv;
+                    }
+                }
+                if (cs.active && cs.kq == 0) {
+                    // final state of rows r0 = rt*16+g and r1 = r0+8 over this item's keys.
+                    // Output columns in pairs: pair pi of this lane holds dims
+                    // (col, col+1) -- bf16 ring: tile pi; fp8 ring: the even and
+                    // odd tiles of dim group pi/2 (see the header comment)
+                    auto pair_of = [&](int pi, int half, float &x, float &y) -> int {
+                        if constexpr (FP8) {
+                            const int grp = pi >> 1, e = pi & 1;
+                            x = cs.o[2 * grp][2 * half + e];
+                            y = cs.o[2 * grp + 1][2 * half + e];
+                            return grp * 16 + 4 * t + 2 * e;
+                        } else {
+                            x = cs.o[pi][2 * half];
+                            y = cs.o[pi][2 * half + 1];
+                            return pi * 8 + 2 * t;
+                        }
+                    };
+    #pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int r = cs.rt * 16 + g + half * 8;
+                        if (r >= cs.R) continue;
+                        const float l = half ? l1 : l0;
+                        const float m = half ? cs.m1 : cs.m0;
+                        const float inv = l > 0.f ? cs.vsc / l : 0.f;
+                        const float lse_v = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+                        const int tok = cs.tok0 + r / p.group;
+                        const int hq = cs.h * p.group + r % p.group;
+                        const int64_t row = static_cast<int64_t>(tok) * p.num_q_heads + hq;
+                        if (cs.nsplit == 1) {
+                            float wa = 1.f, wb = 0.f, lse_f = lse_v;
+                            const float *xo = nullptr;
                             if (p.extra_o) {
-                                x *= wa;
-                                y *= wa;
-                                if (xo) {
-                                    const float2 e2 = __ldg(reinterpret_cast<const float2 *>(xo + col));
-                                    x += wb * e2.x;
-                                    y += wb * e2.y;
+                                const float xl = __ldg(p.extra_lse + row);
+                                const float M = fmaxf(lse_v, xl);
+                                if (M == -INFINITY) {
+                                    wa = 0.f;
+                                } else {
+                                    const float ea = __expf(lse_v - M), eb = __expf(xl - M);
+                                    wa = ea / (ea + eb);
+                                    wb = eb / (ea + eb);
+                                    lse_f = M + __logf(ea + eb);
+                                    xo = p.extra_o + row * D;
                                 }
                             }
-                            dst[col >> 1] = pack_bf16x2(x, y);
+                            uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + row * D);
+    #pragma unroll
+                            for (int pi = 0; pi < NT; ++pi) {
+                                float x, y;
+                                const int col = pair_of(pi, half, x, y);
+                                x *= inv;
+                                y *= inv;
+                                if (p.extra_o) {
+                                    x *= wa;
+                                    y *= wa;
+                                    if (xo) {
+                                        const float2 e2 = __ldg(reinterpret_cast<const float2 *>(xo + col));
+                                        x += wb * e2.x;
+                                        y += wb * e2.y;
+                                    }
+                                }
+                                dst[col >> 1] = pack_bf16x2(x, y);
+                            }
+                            if (p.lse && t == 0) p.lse[row] = lse_f;
+                        } else {
+                            float *dst = p.partial_o + static_cast<int64_t>(cs.partial_base + r) * D;
+    #pragma unroll
+                            for (int pi = 0; pi < NT; ++pi) {
+                                float x, y;
+                                const int col = pair_of(pi, half, x, y);
+                                __stcg(reinterpret_cast<float2 *>(dst + col), make_float2(x * inv, y * inv));
+                            }
+                            if (t == 0) __stcg(p.partial_lse + cs.partial_base + r, lse_v);
                         }
-                        if (p.lse && t == 0) p.lse[row] = lse_f;
-                    } else {
-                        float *dst = p.partial_o + static_cast<int64_t>(cs.partial_base + r) * D;
-#pragma unroll
-                        for (int pi = 0; pi < NT; ++pi) {
-                            float x, y;
-                            const int col = pair_of(pi, half, x, y);
-                            __stcg(reinterpret_cast<float2 *>(dst + col), make_float2(x * inv, y * inv));
-                        }
-                        if (t == 0) __stcg(p.partial_lse + cs.partial_base + r, lse_v);
                     }
                 }
             }
