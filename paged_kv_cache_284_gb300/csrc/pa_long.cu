@@ -100,6 +100,34 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Packed pairs of fp32 (one 64-bit register pair) for the two-wide FMA / add
+// of this architecture, and the three-input maximum: the softmax warps are
+// bound by instruction issue, so each score costs half an FMA, half an add,
+// half a conversion, half a maximum and one exponential.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Everything one role needs to know about a work item.
 struct Item {
     int b, h, tok0, nvalid, pos0, key_begin, key_end, causal, nsplit, split;
@@ -457,11 +485,11 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                 }
                 float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    mx0 = fmaxf(mx0, __uint_as_float(s0[i]));
-                    mx1 = fmaxf(mx1, __uint_as_float(s0[16 + i]));
-                    mx2 = fmaxf(mx2, __uint_as_float(s1[i]));
-                    mx3 = fmaxf(mx3, __uint_as_float(s1[16 + i]));
+                for (int i = 0; i < 16; i += 2) {
+                    mx0 = max3(mx0, __uint_as_float(s0[i]), __uint_as_float(s0[i + 1]));
+                    mx1 = max3(mx1, __uint_as_float(s0[16 + i]), __uint_as_float(s0[17 + i]));
+                    mx2 = max3(mx2, __uint_as_float(s1[i]), __uint_as_float(s1[i + 1]));
+                    mx3 = max3(mx3, __uint_as_float(s1[16 + i]), __uint_as_float(s1[17 + i]));
                 }
                 float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
                 float other;
@@ -484,37 +512,34 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                 }
                 tc_fence_after();
                 const uint32_t pdst = t_lane + G::kColP + sb * (kLongKeys / 2) + half * 32;
-                float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
-                {
+                const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+                const uint64_t nr2 = f2_pack(neg_ref, neg_ref);
+                uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+                for (int piece = 0; piece < 2; ++piece) {
+                    const uint32_t *sv = piece ? s1 : s0;
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; i += 2) {
-                        const float a0 = fast_exp2(fmaf(__uint_as_float(s0[2 * i]), p.scale_log2, neg_ref));
-                        const float a1 = fast_exp2(fmaf(__uint_as_float(s0[2 * i + 1]), p.scale_log2, neg_ref));
-                        const float a2 = fast_exp2(fmaf(__uint_as_float(s0[2 * i + 2]), p.scale_log2, neg_ref));
-                        const float a3 = fast_exp2(fmaf(__uint_as_float(s0[2 * i + 3]), p.scale_log2, neg_ref));
-                        sum0 += a0 + a1;
-                        sum1 += a2 + a3;
+                        float a0, a1, a2, a3;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
+                                         sc2, nr2), a0, a1);
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * i + 2]), __uint_as_float(sv[2 * i + 3])),
+                                         sc2, nr2), a2, a3);
+                        a0 = fast_exp2(a0);
+                        a1 = fast_exp2(a1);
+                        a2 = fast_exp2(a2);
+                        a3 = fast_exp2(a3);
+                        acc0 = f2_add(acc0, f2_pack(a0, a1));
+                        acc1 = f2_add(acc1, f2_pack(a2, a3));
                         pk[i] = pack_bf16x2(a0, a1);
                         pk[i + 1] = pack_bf16x2(a2, a3);
                     }
-                    tmem_st16(pdst, pk);
+                    tmem_st16(pdst + piece * 16, pk);
                 }
-                {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; i += 2) {
-                        const float b0 = fast_exp2(fmaf(__uint_as_float(s1[2 * i]), p.scale_log2, neg_ref));
-                        const float b1 = fast_exp2(fmaf(__uint_as_float(s1[2 * i + 1]), p.scale_log2, neg_ref));
-                        const float b2 = fast_exp2(fmaf(__uint_as_float(s1[2 * i + 2]), p.scale_log2, neg_ref));
-                        const float b3 = fast_exp2(fmaf(__uint_as_float(s1[2 * i + 3]), p.scale_log2, neg_ref));
-                        sum2 += b0 + b1;
-                        sum3 += b2 + b3;
-                        pk[i] = pack_bf16x2(b0, b1);
-                        pk[i + 1] = pack_bf16x2(b2, b3);
-                    }
-                    tmem_st16(pdst + 16, pk);
-                }
+                float sum0, sum1, sum2, sum3;
+                f2_unpack(acc0, sum0, sum1);
+                f2_unpack(acc1, sum2, sum3);
                 l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
                 if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
                     // O is rescaled in place: the previous tile's P V must be done
