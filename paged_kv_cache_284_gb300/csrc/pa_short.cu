@@ -24,7 +24,7 @@
 //    state can be folded in the same epilogue.
 //  * FP8 pool (same page, §02 推理优化: KV-cache quantisation): K and V are
 //    e4m3 codes, one 16-key x 128-dim TMA box per chunk (half the bytes of
-//    bf16).  The MMAs run in f16: e4m3 decodes exactly to f16, q is
+//    bf16), 8 chunks (128 keys) per ring stage.  The MMAs run in f16: e4m3 decodes exactly to f16, q is
 //    converted once per item, P is packed as f16.  K fragments come from
 //    plain ldmatrix (each lane gets 4 consecutive dims of one key; q's dims
 //    are permuted the same way inside each 16-dim k-step, which leaves the
@@ -52,16 +52,20 @@ struct ShortGeom {
     static constexpr int kHalves = FP8 ? 1 : D / 64;          // TMA boxes per 16-key chunk
     static constexpr int kBoxBytes = kChunkKeys * 128;        // 16 rows x 128 B
     static constexpr int kChunkBytes = kHalves * kBoxBytes;   // one 16-key chunk of K (or V)
-    static constexpr int kStageBytes = 2 * kStageChunks * kChunkBytes;
-    static constexpr int kStages = FP8 ? 5 : kShortStages;  // ring depth
-    // merge scratch (per writer warp): 16 rows x D floats + 16 m + 16 l; the
-    // bf16 ring is large enough to hold it in the stage being released, the
-    // fp8 ring is not and gets an area of its own
+    // A ring stage holds 32 KB of K and V: 4 chunks (64 keys) of bf16, or 8
+    // chunks (128 keys, two of the planner's 64-key stages) of e4m3, so that a
+    // consumer warp of an fp8 decode item works on two chunks at once.
+    static constexpr int kCPS = FP8 ? 8 : kStageChunks;       // chunks per ring stage
+    static constexpr int kPSR = kCPS / kStageChunks;          // planner stages per ring stage
+    static constexpr int kRSB = 32 / kCPS;                    // ring stages per block-id batch
+    static constexpr int kStageBytes = 2 * kCPS * kChunkBytes;
+    static constexpr int kStages = kShortStages;              // ring depth
+    // merge scratch (per writer warp): 16 rows x D floats + 16 m + 16 l, kept
+    // in the stage being released
     static constexpr int kScratchFloats = 16 * D + 32;
-    static constexpr int kScratchBytes = FP8 ? 3 * kScratchFloats * 4 : 0;
     static constexpr int kCtlBytes = 512;
-    static constexpr int kSmemBytes = kStages * kStageBytes + kScratchBytes + kCtlBytes + 1024;
-    static_assert(FP8 || 3 * kScratchFloats * 4 <= kStageBytes, "merge scratch must fit one stage");
+    static constexpr int kSmemBytes = kStages * kStageBytes + kCtlBytes + 1024;
+    static_assert(3 * kScratchFloats * 4 <= kStageBytes, "merge scratch must fit one stage");
 };
 
 struct StageMeta {
@@ -132,51 +136,68 @@ __device__ __forceinline__ ShortItem short_work(const ShortParams &p, int idx, i
     return load_record(p.items, rec);
 }
 
-// One 16-key chunk of an fp8 item with at most 8 rows, operands swapped.
+// NC (1 or 2) 16-key chunks of an fp8 item with at most 8 rows, operands
+// swapped; two chunks are interleaved so their dependency chains overlap.
 // Lane (g = lane/4, t = lane%4) holds scores of keys g, g+8 for rows 2t,
 // 2t+1, and O^T tile cc's elements (dim 16cc+2g | 16cc+2g+1) x (row 2t |
 // 2t+1): cs.o[cc][0] = (row 2t, dim 16cc+2g), [1] = (2t+1, 16cc+2g),
 // [2] = (2t, 16cc+2g+1), [3] = (2t+1, 16cc+2g+1).
-template <int D>
-__device__ __forceinline__ void swapped_chunk(Consumer<D> &cs, uint32_t kb, uint32_t vb, int key0,
-                                              int lane) {
+template <int D, int NC>
+__device__ __forceinline__ void swapped_chunks(Consumer<D> &cs, const uint32_t (&kb)[NC],
+                                               const uint32_t (&vb)[NC], const int (&key0)[NC],
+                                               int lane) {
     constexpr int KS = D / 16;
     const int g = lane >> 2, t = lane & 3, mi = lane >> 3;
-    // S^T = K Q^T, two accumulators (even / odd k-steps) for shorter chains
-    float st[2][4];
+    // S^T = K Q^T, two accumulators per chunk (even / odd k-steps)
+    float st[NC][2][4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+    for (int n = 0; n < NC; ++n)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) st[h][e] = 0.f;
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) st[n][h][e] = 0.f;
 #pragma unroll
     for (int ks2 = 0; ks2 < KS / 2; ++ks2) {
         // matrices: keys 0-7 | 8-15 of k-step 2ks2, then of 2ks2+1
         const int key = (mi & 1) * 8 + (lane & 7);
         const int col = ks2 * 2 + (mi >> 1);
-        uint32_t r[4];
-        ldsm_x4(kb + sw128_offset(key, col), r[0], r[1], r[2], r[3]);
+        uint32_t r[NC][4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t a0, a1, a2, a3;
-            e4m3x4_to_f16x2x2(r[2 * h], a0, a2);      // key g:   dims 4t,4t+1 | 4t+2,4t+3
-            e4m3x4_to_f16x2x2(r[2 * h + 1], a1, a3);  // key g+8
-            const int ks = ks2 * 2 + h;
-            mma_f16_16816(st[h], a0, a1, a2, a3, cs.qa[ks][0], cs.qa[ks][1]);
-        }
+        for (int n = 0; n < NC; ++n)
+            ldsm_x4(kb[n] + sw128_offset(key, col), r[n][0], r[n][1], r[n][2], r[n][3]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int n = 0; n < NC; ++n) {
+                uint32_t a0, a1, a2, a3;
+                e4m3x4_to_f16x2x2(r[n][2 * h], a0, a2);      // key g:   dims 4t,4t+1 | 4t+2,4t+3
+                e4m3x4_to_f16x2x2(r[n][2 * h + 1], a1, a3);  // key g+8
+                const int ks = ks2 * 2 + h;
+                mma_f16_16816(st[n][h], a0, a1, a2, a3, cs.qa[ks][0], cs.qa[ks][1]);
+            }
     }
-    float s[4];
-    const bool need_mask = (key0 + kChunkKeys - 1 > cs.ctx) || (key0 + kChunkKeys > cs.key_end);
+    float s[NC][4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        s[e] = (st[0][e] + st[1][e]) * cs.sl2;
-        if (need_mask) {
-            const int key = key0 + g + (e >> 1) * 8;
-            const int lim = (e & 1) ? cs.limit1 : cs.limit0;
-            if (key > lim || key >= cs.key_end) s[e] = -INFINITY;
+    for (int n = 0; n < NC; ++n) {
+        const bool need_mask =
+            (key0[n] + kChunkKeys - 1 > cs.ctx) || (key0[n] + kChunkKeys > cs.key_end);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            s[n][e] = (st[n][0][e] + st[n][1][e]) * cs.sl2;
+            if (need_mask) {
+                const int key = key0[n] + g + (e >> 1) * 8;
+                const int lim = (e & 1) ? cs.limit1 : cs.limit0;
+                if (key > lim || key >= cs.key_end) s[n][e] = -INFINITY;
+            }
         }
     }
     // lazy max: reduce over the 8 lanes of a row only when needed
-    const float la = fmaxf(s[0], s[2]), lb = fmaxf(s[1], s[3]);
+    float la = -INFINITY, lb = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < NC; ++n) {
+        la = fmaxf(la, fmaxf(s[n][0], s[n][2]));
+        lb = fmaxf(lb, fmaxf(s[n][1], s[n][3]));
+    }
     const bool ua = la > cs.m0 + kRescaleThreshold || (cs.m0 == -INFINITY && la > -INFINITY);
     const bool ub = lb > cs.m1 + kRescaleThreshold || (cs.m1 == -INFINITY && lb > -INFINITY);
     if (__any_sync(0xffffffffu, ua || ub)) {
@@ -204,45 +225,60 @@ __device__ __forceinline__ void swapped_chunk(Consumer<D> &cs, uint32_t kb, uint
     }
     const float ref0 = cs.m0 == -INFINITY ? 0.f : cs.m0;
     const float ref1 = cs.m1 == -INFINITY ? 0.f : cs.m1;
-    const float p0 = exp2f(s[0] - ref0), p1 = exp2f(s[1] - ref1);
-    const float p2 = exp2f(s[2] - ref0), p3 = exp2f(s[3] - ref1);
-    cs.l0 += p0 + p2;
-    cs.l1 += p1 + p3;
     // P^T fragments (key g | g+8) x (rows 2t, 2t+1) -> P fragments of row g
-    const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
-    const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
+    uint32_t pb0[NC], pb1[NC];
+#pragma unroll
+    for (int n = 0; n < NC; ++n) {
+        const float p0 = exp2f(s[n][0] - ref0), p1 = exp2f(s[n][1] - ref1);
+        const float p2 = exp2f(s[n][2] - ref0), p3 = exp2f(s[n][3] - ref1);
+        cs.l0 += p0 + p2;
+        cs.l1 += p1 + p3;
+        pb0[n] = movmatrix_trans(pack_f16x2(p0, p1));
+        pb1[n] = movmatrix_trans(pack_f16x2(p2, p3));
+    }
     // O^T += V^T P^T; V rows past the item's keys are zeroed in the fragments
-    const int nvalid = cs.key_end - key0;
-    const bool tail = nvalid < kChunkKeys;
-    const bool k0 = 2 * t < nvalid, k1 = 2 * t + 1 < nvalid;
-    const bool k8 = 2 * t + 8 < nvalid, k9 = 2 * t + 9 < nvalid;
+    bool tail[NC], k0[NC], k1[NC], k8[NC], k9[NC];
+#pragma unroll
+    for (int n = 0; n < NC; ++n) {
+        const int nvalid = cs.key_end - key0[n];
+        tail[n] = nvalid < kChunkKeys;
+        k0[n] = 2 * t < nvalid;
+        k1[n] = 2 * t + 1 < nvalid;
+        k8[n] = 2 * t + 8 < nvalid;
+        k9[n] = 2 * t + 9 < nvalid;
+    }
 #pragma unroll
     for (int c2 = 0; c2 < D / 32; ++c2) {
         // matrices: keys 0-7 | 8-15 of dim group 2c2, then of 2c2+1; lane:
         // keys 2t, 2t+1 x dims 2g, 2g+1 of the group
         const int key = (mi & 1) * 8 + (lane & 7);
         const int col = c2 * 2 + (mi >> 1);
-        uint32_t r[4];
-        ldsm_x4_t(vb + sw128_offset(key, col), r[0], r[1], r[2], r[3]);
-        if (tail) {
-            r[0] = keep_pair(r[0], k0, k1);
-            r[2] = keep_pair(r[2], k0, k1);
-            r[1] = keep_pair(r[1], k8, k9);
-            r[3] = keep_pair(r[3], k8, k9);
+        uint32_t r[NC][4];
+#pragma unroll
+        for (int n = 0; n < NC; ++n) {
+            ldsm_x4_t(vb[n] + sw128_offset(key, col), r[n][0], r[n][1], r[n][2], r[n][3]);
+            if (tail[n]) {
+                r[n][0] = keep_pair(r[n][0], k0[n], k1[n]);
+                r[n][2] = keep_pair(r[n][2], k0[n], k1[n]);
+                r[n][1] = keep_pair(r[n][1], k8[n], k9[n]);
+                r[n][3] = keep_pair(r[n][3], k8[n], k9[n]);
+            }
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t a0, a1, a2, a3;
-            // low halves: dim 16cc+2g (A row g), high: 16cc+2g+1 (A row g+8)
-            e4m3x4_to_f16x2x2(byte_perm(r[2 * h], 0x3120u), a0, a1);
-            e4m3x4_to_f16x2x2(byte_perm(r[2 * h + 1], 0x3120u), a2, a3);
-            mma_f16_16816(cs.o[2 * c2 + h], a0, a1, a2, a3, pb0, pb1);
-        }
+        for (int n = 0; n < NC; ++n)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t a0, a1, a2, a3;
+                // low halves: dim 16cc+2g (A row g), high: 16cc+2g+1 (A row g+8)
+                e4m3x4_to_f16x2x2(byte_perm(r[n][2 * h], 0x3120u), a0, a1);
+                e4m3x4_to_f16x2x2(byte_perm(r[n][2 * h + 1], 0x3120u), a2, a3);
+                mma_f16_16816(cs.o[2 * c2 + h], a0, a1, a2, a3, pb0[n], pb1[n]);
+            }
     }
 }
 
 // Item epilogue of a swapped fp8 item: row sums over the 8 lanes of a row,
-// the 4 consumer warps merged through the merge area, then warp 0 writes
+// the 4 consumer warps merged through the stage buffer, then warp 0 writes
 // rows 2t and 2t+1 (output or partial state).  A cascade prefix state is
 // never folded here: cascade calls take bf16 pools only.
 template <int D>
@@ -341,9 +377,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *stage_mem = smem;
-    float *own_scratch = reinterpret_cast<float *>(smem + kStages * G::kStageBytes);
-    uint64_t *full =
-        reinterpret_cast<uint64_t *>(smem + kStages * G::kStageBytes + G::kScratchBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * G::kStageBytes);
     uint64_t *empty = full + kStages;
     StageMeta *meta = reinterpret_cast<StageMeta *>(empty + kStages);
     int *ctl = reinterpret_cast<int *>(meta + kStages);
@@ -372,7 +406,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
         return stage_mem + slot * G::kStageBytes + (c * G::kHalves + hf) * G::kBoxBytes;
     };
     auto v_box = [&](int slot, int c, int hf) -> uint8_t * {
-        return stage_mem + slot * G::kStageBytes + kStageChunks * G::kChunkBytes +
+        return stage_mem + slot * G::kStageBytes + G::kCPS * G::kChunkBytes +
                (c * G::kHalves + hf) * G::kBoxBytes;
     };
 
@@ -415,19 +449,21 @@ __global__ void __launch_bounds__(kShortThreads, 2)
             if (lane == 0) nxt_idx = atomicAdd(&p.hdr->short_next, 1);  // read two stages later
             ShortItem nxt{};
             int nxt_h = 0, nxt_L = 0, nxt_row = -1, pf = 0;  // prefetch state of the next item
-            const int nst = cur.stage_end - cur.stage_begin;
+            const int nst = cur.stage_end - cur.stage_begin;  // planner stages
+            const int nrs = (nst + G::kPSR - 1) / G::kPSR;     // ring stages
             int batch_row = cur_row, next_batch = -1;
-            for (int rel = 0; rel < nst; ++rel, ++it) {
-                const int st = cur.stage_begin + rel;
-                if ((rel & 7) == 0) {
+            for (int rel = 0; rel < nrs; ++rel, ++it) {
+                const int st = cur.stage_begin + rel * G::kPSR;  // its first planner stage
+                if (rel % G::kRSB == 0) {
                     if (rel > 0) batch_row = next_batch;
-                    next_batch =
-                        (rel + 8 < nst) ? chunk_row_of(p, cur, cur_h, cur_L, st + 8, lane) : -1;
+                    next_batch = (rel + G::kRSB < nrs)
+                                     ? chunk_row_of(p, cur, cur_h, cur_L, st + 8, lane)
+                                     : -1;
                 }
-                // lane c < 4 takes the row of chunk c of this stage
-                const int crow =
-                    __shfl_sync(0xffffffffu, batch_row, (rel & 7) * kStageChunks + (lane & 3));
-                const int nvalid = __popc(__ballot_sync(0xffffffffu, lane < kStageChunks && crow >= 0));
+                // lane c < kCPS takes the row of chunk c of this stage
+                const int crow = __shfl_sync(0xffffffffu, batch_row,
+                                             (rel % G::kRSB) * G::kCPS + (lane % G::kCPS));
+                const int nvalid = __popc(__ballot_sync(0xffffffffu, lane < G::kCPS && crow >= 0));
                 const int slot = it % kStages;
                 int ok = 1;
                 if (lane == 0 && it >= kStages)
@@ -441,15 +477,15 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                     StageMeta mm;
                     mm.item = cur_idx;
                     mm.stage = st;
-                    mm.flags = (rel == 0 ? kFirst : 0) | (rel == nst - 1 ? kLast : 0);
+                    mm.flags = (rel == 0 ? kFirst : 0) | (rel == nrs - 1 ? kLast : 0);
                     mm.pad = 0;
                     meta[slot] = mm;
                     mbar_arrive_expect_tx(&full[slot],
                                           static_cast<uint32_t>(nvalid * 2 * G::kChunkBytes));
                 }
                 __syncwarp();
-                // the four chunks' copies are issued by four lanes at once
-                if (lane < kStageChunks && crow >= 0) {
+                // the stage's chunks' copies are issued by one lane each, at once
+                if (lane < G::kCPS && crow >= 0) {
 #pragma unroll
                     for (int hf = 0; hf < G::kHalves; ++hf) {
                         tma_load_2d(k_box(slot, lane, hf), &tmk, hf * 64, crow, &full[slot]);
@@ -460,21 +496,21 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                 // one prefetch step per stage from the third stage on; the last
                 // stage finishes whatever is left
                 for (;;) {
-                    if (pf == 0 && (rel >= 2 || rel == nst - 1)) {
+                    if (pf == 0 && (rel >= 2 || rel == nrs - 1)) {
                         nxt_idx = __shfl_sync(0xffffffffu, nxt_idx, 0);
                         if (nxt_idx < num_items) nxt = short_work(p, nxt_idx, nxt_h);
                         pf = 1;
-                    } else if (pf == 1 && (rel >= 3 || rel == nst - 1)) {
+                    } else if (pf == 1 && (rel >= 3 || rel == nrs - 1)) {
                         if (nxt_idx < num_items) nxt_L = __ldg(p.seq_lens + nxt.b);
                         pf = 2;
-                    } else if (pf == 2 && (rel >= 4 || rel == nst - 1)) {
+                    } else if (pf == 2 && (rel >= 4 || rel == nrs - 1)) {
                         if (nxt_idx < num_items)
                             nxt_row = chunk_row_of(p, nxt, nxt_h, nxt_L, nxt.stage_begin, lane);
                         pf = 3;
                     } else {
                         break;
                     }
-                    if (rel != nst - 1) break;
+                    if (rel != nrs - 1) break;
                 }
             }
             if (aborted) break;
@@ -607,19 +643,37 @@ __global__ void __launch_bounds__(kShortThreads, 2)
         }
 
         // ---- process this warp's chunks of the stage ----
-        if (cs.active) {
-            for (int c = cs.kq; c < kStageChunks; c += cs.KQ) {
+        bool done_swapped = false;
+        if constexpr (FP8) {
+            if (cs.swapped) {
+                // a warp's two chunks of the stage (kq and kq + 4), together
+                done_swapped = true;
+                const int ka = (mm.stage * kStageChunks + cs.kq) * kChunkKeys;
+                const int kb2 = ka + cs.KQ * kChunkKeys;
+                if (ka < cs.key_end) {
+                    if (kb2 < cs.key_end) {
+                        const uint32_t kbs[2] = {smem_u32(k_box(slot, cs.kq, 0)),
+                                                 smem_u32(k_box(slot, cs.kq + cs.KQ, 0))};
+                        const uint32_t vbs[2] = {smem_u32(v_box(slot, cs.kq, 0)),
+                                                 smem_u32(v_box(slot, cs.kq + cs.KQ, 0))};
+                        const int ks0[2] = {ka, kb2};
+                        swapped_chunks<D, 2>(cs, kbs, vbs, ks0, lane);
+                    } else {
+                        const uint32_t kbs[1] = {smem_u32(k_box(slot, cs.kq, 0))};
+                        const uint32_t vbs[1] = {smem_u32(v_box(slot, cs.kq, 0))};
+                        const int ks0[1] = {ka};
+                        swapped_chunks<D, 1>(cs, kbs, vbs, ks0, lane);
+                    }
+                }
+            }
+        }
+        if (cs.active && !done_swapped) {
+            for (int c = cs.kq; c < G::kCPS; c += cs.KQ) {
                 const int key0 = (mm.stage * kStageChunks + c) * kChunkKeys;
                 if (key0 >= cs.key_end) break;
                 const uint32_t kb = smem_u32(k_box(slot, c, 0));
                 const uint32_t vb = smem_u32(v_box(slot, c, 0));
                 const int mi = lane >> 3;
-                if constexpr (FP8) {
-                    if (cs.swapped) {
-                        swapped_chunk<D>(cs, kb, vb, key0, lane);
-                        continue;
-                    }
-                }
                 float sacc[2][4];
 #pragma unroll
                 for (int i = 0; i < 2; ++i)
@@ -769,16 +823,17 @@ __global__ void __launch_bounds__(kShortThreads, 2)
         if (mm.flags & kLast) {
             // ---- item epilogue ----
             if (FP8 && cs.swapped) {
-                swapped_epilogue<D>(cs, p, own_scratch, lane, warp);
+                swapped_epilogue<D>(cs, p, reinterpret_cast<float *>(stage_mem + slot * G::kStageBytes),
+                                    lane, warp);
+                wrote_stage = true;
             } else {
                 float l0 = quad_sum(cs.l0), l1 = quad_sum(cs.l1);
                 if (cs.KQ > 1) {
                     // merge the KQ warps that share a row tile, through this
-                    // stage's buffer (bf16 ring) or the merge area (fp8 ring)
+                    // stage's buffer
                     named_bar_sync(1, 32 * kShortConsumerWarps);
-                    float *scratch = FP8 ? own_scratch
-                                         : reinterpret_cast<float *>(stage_mem + slot * G::kStageBytes);
-                    wrote_stage = !FP8;
+                    float *scratch = reinterpret_cast<float *>(stage_mem + slot * G::kStageBytes);
+                    wrote_stage = true;
                     if (cs.active && cs.kq > 0) {
                         float *reg = scratch + (cs.rt * (cs.KQ - 1) + cs.kq - 1) * G::kScratchFloats;
     #pragma unroll
