@@ -80,9 +80,11 @@ enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 };
  * (v_scale[h] for V).  The scales are the caller's; they must be finite and
  * positive.  head_dim must be 128.  Attention over an fp8 pool computes q in
  * f16 (|q| must stay below 65504), K and V as decoded exactly to f16 and
- * scaled in fp32; all rows run on the split-KV kernel (longer requests in
- * pieces of 64 / group query tokens).  pa_prefix_attention and
- * pa_cascade_decode accept bf16 pools only.
+ * scaled in fp32 on the split-KV kernel.  Requests with q_len * group > 64
+ * run on the tensor-core kernel over a bf16 copy of their blocks when the
+ * workspace has room for it (pa_fp8_staging_bytes), and on the split-KV
+ * kernel in pieces of 64 / group query tokens otherwise.
+ * pa_prefix_attention and pa_cascade_decode accept bf16 pools only.
  */
 typedef struct pa_kv_desc {
     void *k_cache;
@@ -125,6 +127,20 @@ int pa_write_kv(const void *k, const void *v, const int64_t *slot_mapping, int32
  */
 size_t pa_attention_workspace_size(int32_t num_seqs, int32_t num_q_tokens, int32_t num_q_heads,
                                    int32_t num_kv_heads, int32_t head_dim);
+
+/*
+ * Extra workspace bytes, on top of pa_attention_workspace_size, that let an
+ * fp8 (e4m3) pool run its long requests (q_len * group > 64) on the
+ * tensor-core kernel: num_blocks bf16 blocks of K and of V, i.e. the blocks
+ * of the step's long requests (sum of ceil(seq_len / block_size)).  Any
+ * workspace beyond the step's own layout serves as this staging area;
+ * pa_attention decodes the long requests' blocks into it (exactly: every
+ * e4m3 value is a bf16 value; the scales stay separate) in request order
+ * while they fit, and runs the rest as split-KV pieces.  Returns 0 for
+ * invalid sizes.  bf16 pools ignore any extra workspace.
+ */
+size_t pa_fp8_staging_bytes(int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            int64_t num_blocks);
 
 /*
  * Varlen paged attention for one continuous-batching step ([TC], [CH]).

@@ -35,7 +35,7 @@ EXPORTED = ["pa_write_kv", "pa_attention_workspace_size", "pa_attention", "pa_at
             "pa_merge_states", "pa_cascade_workspace_size", "pa_prefix_attention",
             "pa_cascade_decode", "pa_validate_metadata", "pa_last_error_message",
             "pa_status_string", "pa_read_device_status", "pa_set_profile_events",
-            "pa_attention_no_alloc",
+            "pa_attention_no_alloc", "pa_fp8_staging_bytes",
             # block manager (include/pa_blocks.h)
             "pa_bm_create", "pa_bm_destroy", "pa_bm_add_request", "pa_bm_append_tokens",
             "pa_bm_fork", "pa_bm_schedule", "pa_bm_free_request", "pa_bm_num_free_blocks",
@@ -89,6 +89,7 @@ def _declare(lib):
         "pa_set_profile_events": ([i32, P, P], ctypes.c_int),
         "pa_attention_no_alloc": ([P, KV, P, i32, P, P, P, i32, i32, i32, f32, P, P, P],
                                   ctypes.c_int),
+        "pa_fp8_staging_bytes": ([i32, i32, i32, i64], sz),
         "pa_bm_create": ([i32, i32], P),
         "pa_bm_destroy": ([P], None),
         "pa_bm_add_request": ([P, i64, P, i32, P], ctypes.c_int),
@@ -209,12 +210,18 @@ def alloc_workspace(nbytes: int, device=None) -> torch.Tensor:
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device or "cuda")
 
 
+def fp8_staging_bytes(num_kv_heads, head_dim, block_size, num_blocks) -> int:
+    return int(lib().pa_fp8_staging_bytes(num_kv_heads, head_dim, block_size, int(num_blocks)))
+
+
 def pa_attention(q, k_cache, v_cache, block_tables, query_start_loc, context_lens, seq_lens,
                  scale, out, lse=None, workspace=None, stream=None, short_q_max_rows=-1,
-                 split_keys=0, k_scale=None, v_scale=None):
+                 split_keys=0, k_scale=None, v_scale=None, staging_blocks=0):
     """Varlen paged attention for one step; writes out (bf16 [T,Hq,d]) and lse
     (fp32 [T,Hq], optional).  An fp8 pool takes k_scale / v_scale (fp32
-    [Hkv]).  Returns the workspace tensor used."""
+    [Hkv]); a workspace allocated here gets room to stage staging_blocks
+    blocks of its long requests for the tensor-core kernel (a caller's
+    workspace is used as given).  Returns the workspace tensor used."""
     _need(q, "q", torch.bfloat16)
     _need(out, "out", torch.bfloat16)
     for name, t in (("block_tables", block_tables), ("query_start_loc", query_start_loc),
@@ -226,6 +233,8 @@ def pa_attention(q, k_cache, v_cache, block_tables, query_start_loc, context_len
     T, hq, _ = q.shape
     B = int(seq_lens.shape[0])
     need = workspace_size(B, T, hq, kv.num_kv_heads, kv.head_dim)
+    if kv.kv_dtype == PA_KV_FP8_E4M3 and staging_blocks > 0:
+        need += fp8_staging_bytes(kv.num_kv_heads, kv.head_dim, kv.block_size, staging_blocks)
     if workspace is None or workspace.numel() < need:
         workspace = alloc_workspace(need, q.device)
     _check(lib().pa_attention_ex(_ptr(q), ctypes.byref(kv), _ptr(block_tables),

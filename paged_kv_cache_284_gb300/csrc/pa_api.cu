@@ -175,6 +175,10 @@ WsLayout make_layout(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv
     off = align256(off + sizeof(float) * static_cast<size_t>(L.cap_rows) * head_dim);
     L.partial_lse = off;
     off = align256(off + sizeof(float) * static_cast<size_t>(L.cap_rows));
+    L.stage_base = off;
+    off = align256(off + sizeof(int) * static_cast<size_t>(num_seqs > 0 ? num_seqs : 1));
+    L.stage_list = off;
+    off = align256(off + sizeof(int) * static_cast<size_t>(num_seqs > 0 ? num_seqs : 1));
     if (with_extra) {
         const size_t rows = static_cast<size_t>(num_q_tokens) * num_q_heads;
         L.extra_o = off;
@@ -233,6 +237,39 @@ struct StepMaps {
     CUtensorMap q, k, v;
 };
 
+// bf16 staging copy of the long requests' blocks of an fp8 pool: the part of
+// the caller's workspace beyond the step's own layout (cap blocks for K and
+// for V, [cap][Hkv][bs][d] each).
+struct Staging {
+    int cap = 0;
+    void *k = nullptr, *v = nullptr;
+    CUtensorMap tk, tv;
+};
+
+size_t stage_block_bytes(const pa_kv_desc *kv) {
+    return static_cast<size_t>(kv->num_kv_heads) * kv->block_size * kv->head_dim * 2;
+}
+
+// Carves the staging area out of workspace bytes [used, total).
+int make_staging(Staging *st, const pa_kv_desc *kv, uint8_t *ws, size_t used, size_t total) {
+    st->cap = 0;
+    if (kv->kv_dtype != PA_KV_FP8_E4M3 || !ws) return PA_OK;
+    const size_t start = align256(used);
+    const size_t blk = stage_block_bytes(kv);
+    if (total < start + 512 + 2 * blk) return PA_OK;
+    size_t cap = (total - start - 512) / (2 * blk);
+    const size_t max_rows = (static_cast<size_t>(1) << 31) - 256;
+    cap = std::min(cap, max_rows / (static_cast<size_t>(kv->num_kv_heads) * kv->block_size));
+    cap = std::min<size_t>(cap, 1u << 28);
+    st->cap = static_cast<int>(cap);
+    st->k = ws + start;
+    st->v = ws + start + align256(cap * blk);
+    const int64_t rows = static_cast<int64_t>(cap) * kv->num_kv_heads * kv->block_size;
+    int rc = make_kv_map(&st->tk, st->k, rows, kv->head_dim, false);
+    if (rc == PA_OK) rc = make_kv_map(&st->tv, st->v, rows, kv->head_dim, false);
+    return rc;
+}
+
 int make_maps(StepMaps *m, const void *q, const pa_kv_desc *kv, int tokens, int heads) {
     const int group = heads / kv->num_kv_heads;
     const bool fp8 = kv->kv_dtype == PA_KV_FP8_E4M3;
@@ -249,8 +286,8 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
              const int32_t *qsl, const int32_t *ctx, const int32_t *seq_lens, int32_t num_seqs,
              int32_t T, int32_t Hq, float scale, void *out, float *lse, uint8_t *ws,
              const WsLayout &L, int short_max_rows, int split_keys, const float *extra_o,
-             const float *extra_lse, bool forbid_long, const StepMaps &maps, DeviceInfo *dev,
-             cudaStream_t s) {
+             const float *extra_lse, bool forbid_long, const StepMaps &maps, const Staging &stg,
+             DeviceInfo *dev, cudaStream_t s) {
     const int D = kv->head_dim;
     const int group = Hq / kv->num_kv_heads;
     const int tq = q_tile_tokens(group);
@@ -265,12 +302,20 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
     pp.num_kv_heads = kv->num_kv_heads;
     pp.group = group;
     pp.q_tile_tokens = tq;
-    // an fp8 pool runs every row on the split-KV kernel; a request longer
-    // than a piece is cut into pieces of piece_tokens query tokens
+    // An fp8 pool runs short rows on the split-KV kernel; long requests run on
+    // the tensor-core kernel over a bf16 staging copy while staging blocks
+    // last, and as split-KV pieces of piece_tokens query tokens otherwise
+    // (all of them when the workspace has no staging area).
     const bool fp8 = kv->kv_dtype == PA_KV_FP8_E4M3;
-    if (fp8) forbid_long = true;
+    const bool staged = fp8 && stg.cap > 0;
+    if (fp8 && !staged) forbid_long = true;
     pp.short_max_rows = forbid_long ? 0x7fffffff : short_max_rows;
     pp.piece_tokens = std::max(1, std::min(pp.short_max_rows, kShortMaxRows) / group);
+    pp.fp8 = fp8 ? 1 : 0;
+    pp.stage_cap = staged ? stg.cap : 0;
+    pp.block_size = kv->block_size;
+    pp.stage_base = staged ? reinterpret_cast<int *>(ws + L.stage_base) : nullptr;
+    pp.stage_list = staged ? reinterpret_cast<int *>(ws + L.stage_list) : nullptr;
     pp.split_stages = split_keys / kStageKeys;
     const int short_grid = dev->sms * dev->short_ctas_per_sm[fp8 ? 2 : (D == 128 ? 1 : 0)];
     pp.target_items = kSplitItemsPerCta * short_grid;
@@ -289,6 +334,11 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
         rc = launch_plan(pp, s);
     }
     if (rc != PA_OK) return fail(rc, "plan launch failed");
+    if (staged) {
+        rc = launch_stage_fp8(kv, block_tables, max_blocks, hdr, pp.stage_base, pp.stage_list,
+                              stg.k, stg.v, dev->status, 2 * dev->sms, s);
+        if (rc != PA_OK) return fail(rc, "fp8 staging copy launch failed");
+    }
 
     ShortParams sp{};
     sp.q = static_cast<const __nv_bfloat16 *>(q);
@@ -349,6 +399,13 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
         lp.partial_o = sp.partial_o;
         lp.partial_lse = sp.partial_lse;
         lp.status = dev->status;
+        if (staged) {
+            lp.stage_base = pp.stage_base;
+            lp.k_scale = kv->k_scale;
+            lp.v_scale = kv->v_scale;
+            lp.num_blocks = stg.cap;
+            lp.kv_rows = stg.cap * kv->num_kv_heads * kv->block_size;
+        }
         // the split-KV kernel was launched just before: the tensor-core grid
         // may take over SMs as split-KV CTAs finish (its rows are disjoint)
         lp.overlap_prev = short_grid > 0 ? 1 : 0;
@@ -359,7 +416,8 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
         const int grid = kv->num_kv_heads * ((T + tq - 1) / tq + max_long_reqs);
         {
             ProfScope prof(PA_KERNEL_TENSOR_CORE, s);
-            rc = launch_long(lp, maps.q, maps.k, maps.v, D, std::min(grid, L.max_long), s);
+            rc = launch_long(lp, maps.q, staged ? stg.tk : maps.k, staged ? stg.tv : maps.v, D,
+                             std::min(grid, L.max_long), s);
         }
         if (rc != PA_OK) return fail(rc, "tensor-core kernel launch failed: %s",
                                      cudaGetErrorString(cudaGetLastError()));
@@ -510,7 +568,7 @@ int attention_in_fixed_workspace(const void *q, const pa_kv_desc *kv,
     return run_step(q, kv, block_tables, max_blocks_per_seq, query_start_loc, context_lens,
                     seq_lens, num_seqs, num_q_tokens, num_q_heads, scale, out, lse,
                     static_cast<uint8_t *>(scratch), L, kShortMaxRows, 0, nullptr, nullptr,
-                    false, maps, dev, s);
+                    false, maps, Staging(), dev, s);
 }
 
 int set_error_message(int code, const char *msg) { return fail(code, "%s", msg); }
@@ -588,11 +646,23 @@ int pa_attention_ex(const void *q, const pa_kv_desc *kv, const int32_t *block_ta
     if ((rc = device_info(&dev)) != PA_OK) return rc;
     StepMaps maps;
     if ((rc = make_maps(&maps, q, kv, num_q_tokens, num_q_heads)) != PA_OK) return rc;
+    // an fp8 pool stages long requests in the workspace beyond the layout
+    Staging stg;
+    if ((rc = make_staging(&stg, kv, static_cast<uint8_t *>(workspace), L.total, workspace_bytes)) !=
+        PA_OK)
+        return rc;
     return run_step(q, kv, block_tables, max_blocks_per_seq, query_start_loc, context_lens,
                     seq_lens, num_seqs, num_q_tokens, num_q_heads, scale, out, lse,
                     static_cast<uint8_t *>(workspace), L,
                     short_q_max_rows < 0 ? kShortMaxRows : short_q_max_rows, split_keys, nullptr,
-                    nullptr, false, maps, dev, static_cast<cudaStream_t>(stream));
+                    nullptr, false, maps, stg, dev, static_cast<cudaStream_t>(stream));
+}
+
+size_t pa_fp8_staging_bytes(int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            int64_t num_blocks) {
+    if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0) return 0;
+    const size_t blk = static_cast<size_t>(num_kv_heads) * block_size * head_dim * 2;
+    return 2 * align256(static_cast<size_t>(num_blocks) * blk) + 768;
 }
 
 int pa_attention(const void *q, const pa_kv_desc *kv, const int32_t *block_tables,
@@ -703,7 +773,7 @@ int pa_cascade_decode(const void *q, const pa_kv_desc *kv, const int32_t *prefix
     if (rc != PA_OK) return rc;
     return run_step(q, kv, block_tables, max_blocks_per_seq, query_start_loc, context_lens,
                     seq_lens, num_seqs, num_q_tokens, num_q_heads, scale, out, lse, ws, L,
-                    kShortMaxRows, 0, xo, xl, true, maps, dev, s);
+                    kShortMaxRows, 0, xo, xl, true, maps, Staging(), dev, s);
 }
 
 int pa_validate_metadata(const int32_t *block_tables, int32_t max_blocks_per_seq,

@@ -45,7 +45,9 @@ struct PlanHeader {
     int long_next;         // dynamic work counter of the tensor-core kernel
     int split_stages;      // chosen split size (in 64-key stages)
     int partial_rows;      // partial-state rows used
-    int pad[10];
+    int num_staged;        // fp8 pool: long requests given a bf16 staging copy
+    int staged_blocks;     // staging blocks used
+    int pad[8];
 };
 static_assert(sizeof(PlanHeader) == 64, "header size");
 
@@ -99,6 +101,7 @@ __device__ __forceinline__ void store_record(T *base, int rec, const T &r) {
 // Byte offsets of the workspace regions (same computation on host and device).
 struct WsLayout {
     size_t header, counters, short_items, long_items, partial_o, partial_lse, extra_o, extra_lse;
+    size_t stage_base, stage_list;  // fp8 staging bookkeeping ([num_seqs] each)
     size_t total;
     int max_short, max_long, cap_rows, num_counters;
 };
@@ -139,6 +142,11 @@ struct LongParams {
     int *counters;
     float *partial_o, *partial_lse;
     unsigned *status;
+    // fp8 pool with a bf16 staging copy: request b's key block j is staging
+    // block stage_base[b] + j (decoded codes, unscaled); scores are scaled by
+    // k_scale[h] and outputs by v_scale[h].  NULL for a bf16 pool.
+    const int *stage_base;
+    const float *k_scale, *v_scale;
     // 1: launched as a programmatic dependent of the split-KV kernel of the
     // same step.  The kernel then reads nothing but the plan's output (and
     // the step's inputs) before its last instruction, where it waits for the
@@ -151,6 +159,12 @@ struct PlanParams {
     int num_seqs, num_q_tokens, num_kv_heads, group, q_tile_tokens;
     int short_max_rows;  // q_len*group <= this -> split-KV kernel
     int piece_tokens;    // a split-KV request is cut into pieces of this many tokens
+    // fp8 pool: long requests (q_len * group > kShortMaxRows) get a bf16
+    // staging copy of their blocks, in request order while stage_cap blocks
+    // last; stage_base[b] = first staging block or -1, stage_list = staged
+    // requests in order.  stage_cap = 0: no staging (all rows split-KV).
+    int fp8, stage_cap, block_size;
+    int *stage_base, *stage_list;
     int split_stages;    // 0 = automatic
     int target_items;    // automatic split aims at about this many split-KV items
     PlanHeader *hdr;
@@ -185,6 +199,11 @@ struct PdlLaunch {
 // Host-side launchers (each defined next to its kernel).
 int launch_write_kv(const void *k, const void *v, const int64_t *slots, int num_tokens,
                     const pa_kv_desc *kv, unsigned *status, cudaStream_t s);
+// Decodes the e4m3 blocks of the staged requests (plan output) into the
+// bf16 staging pool; grid-stride over staging blocks.
+int launch_stage_fp8(const pa_kv_desc *kv, const int32_t *block_tables, int32_t bt_stride,
+                     const PlanHeader *hdr, const int *stage_base, const int *stage_list,
+                     void *stage_k, void *stage_v, unsigned *status, int grid, cudaStream_t s);
 int launch_plan(const PlanParams &p, cudaStream_t s);
 int launch_short(const ShortParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                  int head_dim, bool fp8, int grid, cudaStream_t s);

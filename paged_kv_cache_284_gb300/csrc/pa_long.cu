@@ -224,7 +224,8 @@ __device__ void produce(const LongParams &p, const CUtensorMap *tm, uint8_t *rin
                         flag_status(p.status, PA_DEV_BAD_METADATA);
                         col = p.bt_stride - 1;
                     }
-                    int blk = __ldg(bt + col);
+                    // fp8 pool: block col of a staged request is its staging block
+                    int blk = p.stage_base ? __ldcg(p.stage_base + it.b) + col : __ldg(bt + col);
                     if (blk < 0 || blk >= p.num_blocks) {
                         flag_status(p.status, PA_DEV_BAD_BLOCK);
                         blk = min(max(blk, 0), p.num_blocks - 1);
@@ -458,6 +459,8 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
             const int row_limit = it.causal ? it.pos0 + ttok : 0x7fffffff;
             const int tile_limit_min = it.causal ? it.pos0 : 0x7fffffff;
             float m_used = -INFINITY, l = 0.f;
+            // scores in log2 units; an fp8 pool's K scale folds in here
+            const float sl2 = p.k_scale ? p.scale_log2 * __ldg(p.k_scale + it.h) : p.scale_log2;
             for (int j = 0; ok && j < it.nt; ++j) {
                 const uint32_t tt = t + j;
                 const int sb = tt & 1;
@@ -495,7 +498,7 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                 float other;
                 if (!swap_halves(xch + (tt & 1) * 256, mx, other)) { ok = false; break; }
                 mx = fmaxf(mx, other);
-                const float mxs = mx * p.scale_log2;  // scale > 0: max commutes with it
+                const float mxs = mx * sl2;  // scale > 0: max commutes with it
                 float alpha = 1.f;
                 if (mxs > m_used + kRescaleThreshold || (m_used == -INFINITY && mxs > -INFINITY)) {
                     alpha = m_used == -INFINITY ? 0.f : fast_exp2(m_used - mxs);
@@ -512,7 +515,7 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                 }
                 tc_fence_after();
                 const uint32_t pdst = t_lane + G::kColP + sb * (kLongKeys / 2) + half * 32;
-                const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+                const uint64_t sc2 = f2_pack(sl2, sl2);
                 const uint64_t nr2 = f2_pack(neg_ref, neg_ref);
                 uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
@@ -594,7 +597,9 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
             }
 
             // ---- epilogue of this item: this half's D/2 output columns ----
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            // an fp8 pool's V scale multiplies the output
+            const float vsc = p.v_scale ? __ldg(p.v_scale + it.h) : 1.f;
+            const float inv = l > 0.f ? vsc / l : 0.f;
             const float lse_v = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
             const int tok = it.tok0 + ttok;
             const int hq = it.h * p.group + jh;

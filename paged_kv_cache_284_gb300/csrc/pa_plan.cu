@@ -83,6 +83,8 @@ __device__ __forceinline__ ReqInfo load_req(const PlanParams &p, int b) {
     }
     if (r.n > 0) {
         r.is_short = (static_cast<long long>(r.n) * p.group <= p.short_max_rows) ? 1 : 0;
+        // fp8 pool: a long request without a staging copy runs as pieces
+        if (p.fp8 && !r.is_short && !(p.stage_cap > 0 && p.stage_base[b] >= 0)) r.is_short = 1;
         if (r.is_short)
             r.pieces = (r.n + p.piece_tokens - 1) / p.piece_tokens;
         else
@@ -140,6 +142,32 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         s_max_stages = 0;
     }
     for (int i = tid; i < kSortBins; i += kPlanThreads) bins[i] = 0;
+    // 0. fp8 pool with a staging area: long requests get consecutive bf16
+    // staging blocks in request order while they fit (a request that does
+    // not fit, and every later one, runs as split-KV pieces instead).
+    int staged = 0, staged_blocks = 0;
+    if (p.fp8 && p.stage_cap > 0) {
+        int cand_base = 0;
+        for (int b0 = 0; b0 < p.num_seqs; b0 += kPlanThreads) {
+            const int b = b0 + tid;
+            int cnt = 0;
+            if (b < p.num_seqs) {
+                const int n = p.qsl[b + 1] - p.qsl[b], len = p.seq_lens[b];
+                if (n > 0 && len > 0 && static_cast<long long>(n) * p.group > p.short_max_rows)
+                    cnt = (len + p.block_size - 1) / p.block_size;
+            }
+            int tot_c, tot_s;
+            const int base = cand_base + block_exclusive_scan(cnt, tmp, &tot_c);
+            const bool fits = cnt > 0 && base + cnt <= p.stage_cap;
+            const int idx = staged + block_exclusive_scan(fits ? 1 : 0, tmp, &tot_s);
+            if (b < p.num_seqs) p.stage_base[b] = fits ? base : -1;
+            if (fits) p.stage_list[idx] = b;
+            staged_blocks += static_cast<int>(block_sum_ll(fits ? cnt : 0, tmpl));
+            cand_base += tot_c;
+            staged += tot_s;
+        }
+        __syncthreads();
+    }
     // Request tid's metadata is read once and kept in registers; only steps
     // with more than kPlanThreads requests read the others again per pass.
     const ReqInfo mine = tid < p.num_seqs ? load_req(p, tid) : ReqInfo{};
@@ -316,6 +344,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         p.hdr->long_next = 0;
         p.hdr->split_stages = sp;
         p.hdr->partial_rows = row_base;
+        p.hdr->num_staged = s_overflow ? 0 : staged;
+        p.hdr->staged_blocks = s_overflow ? 0 : staged_blocks;
     }
 }
 

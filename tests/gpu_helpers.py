@@ -110,9 +110,28 @@ def gpu_attend_fp8(step, kc, vc, ks, vs, **kw):
     q = step.q.to(DEV)
     out = torch.full_like(q, float("nan"))
     lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
-    pk.pa_attention(q, kc, vc, scale=step.scale, out=out, lse=lse, k_scale=ks, v_scale=vs,
-                    **dev_meta(step), **kw)
+    ws = pk.pa_attention(q, kc, vc, scale=step.scale, out=out, lse=lse, k_scale=ks, v_scale=vs,
+                         **dev_meta(step), **kw)
+    gpu_attend_fp8.last_workspace = ws
     return out, lse
+
+
+def plan_header(ws):
+    """The step plan's header at the start of the workspace (white-box check):
+    work items of the two kernels and the fp8 staging counts."""
+    h = ws[:64].cpu().view(torch.int32).tolist()
+    return {"short_items": h[0], "long_items": h[1], "num_staged": h[6], "staged_blocks": h[7]}
+
+
+def long_requests(step, short_max_rows=64):
+    """Requests whose q_len * group exceeds the split-KV kernel's rows."""
+    group = step.num_q_heads // step.num_kv_heads
+    return [b for b, n in enumerate(step.q_lens.tolist()) if n * group > short_max_rows]
+
+
+def staging_blocks_for(step, reqs):
+    bs = step.block_size
+    return sum(-(-int(step.seq_lens[b]) // bs) for b in reqs)
 
 
 def run_and_check_fp8(pool8, steps, **kw):

@@ -21,7 +21,7 @@ def declared_functions():
     for h in sorted(os.listdir(inc)):
         if h.endswith(".h"):
             src = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, h)).read(), flags=re.S)
-            names.update(re.findall(r"\b(pa_[a-z_]+)\s*\(", src))
+            names.update(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", src))
     return sorted(names)
 
 

@@ -9,7 +9,8 @@ import oracle
 import paged_kv_cache_284_gb300 as pk
 from paged_kv_cache_284_gb300 import workloads
 from gpu_helpers import (DEV, assert_attention_close, assert_status_clean, codes, fp8_dev,
-                         gpu_attend_fp8, gpu_write_fp8, run_and_check_fp8)
+                         gpu_attend_fp8, gpu_write_fp8, long_requests, plan_header,
+                         run_and_check_fp8, staging_blocks_for)
 
 pytestmark = pytest.mark.gpu
 
@@ -111,3 +112,34 @@ def test_fp8_rejected_where_not_built():
     kc, vc, ks, vs = fp8_dev(pool8)
     with pytest.raises(pk.PaError):
         gpu_write_fp8(step, kc, vc, ks, vs)
+
+
+def test_fp8_long_rows_on_the_tensor_core_path():
+    """With room to stage them, the long requests (chunks, the prefix-hit
+    prompt) run on the tensor-core kernel over a bf16 copy of their blocks;
+    all of them are staged and the results match the oracle."""
+    pool, steps = workloads.chunked_prefix_decode()
+    big_pool, big_steps = workloads.mixed_step(num_chunks=3, chunk_len=96, chunk_ctx=(0, 900),
+                                               num_decode=12, decode_len=(20, 900), num_spec=4,
+                                               spec_ctx=(20, 900))
+    for pool8, stps in ((workloads.fp8_pool_like(pool, 7020), steps),
+                        (workloads.fp8_pool_like(big_pool, 7021), big_steps)):
+        room = max(staging_blocks_for(st, long_requests(st)) for st in stps)
+        run_and_check_fp8(pool8, stps, staging_blocks=room)
+        longs = long_requests(stps[-1])
+        hdr = plan_header(gpu_attend_fp8.last_workspace)
+        assert longs and hdr["num_staged"] == len(longs) and hdr["long_items"] > 0, hdr
+
+
+def test_fp8_partial_staging_splits_long_rows_between_the_paths():
+    """Staging room for only the first long request: it runs on the
+    tensor-core kernel, the later ones as split-KV pieces."""
+    pool, (step,) = workloads.mixed_step(num_chunks=3, chunk_len=64, chunk_ctx=(0, 700),
+                                         num_decode=8, decode_len=(20, 700), num_spec=3,
+                                         spec_ctx=(20, 700))
+    longs = long_requests(step)
+    assert len(longs) == 3
+    first = staging_blocks_for(step, longs[:1])
+    pool8 = workloads.fp8_pool_like(pool, 7022)
+    run_and_check_fp8(pool8, [step], staging_blocks=first)
+    assert plan_header(gpu_attend_fp8.last_workspace)["num_staged"] == 1
