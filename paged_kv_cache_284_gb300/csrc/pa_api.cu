@@ -137,6 +137,13 @@ struct ProfScope {
     }
 };
 
+// True while per-kernel profiling events are set: the step then launches its
+// kernels one after the other so that each event pair times one kernel.
+bool profiling_active() {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    return g_prof[PA_KERNEL_SPLIT_KV][0] || g_prof[PA_KERNEL_TENSOR_CORE][0];
+}
+
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 int q_tile_tokens(int group) { return group <= kLongRows ? kLongRows / group : 0; }
@@ -366,15 +373,15 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
     sp.k_scale = fp8 ? kv->k_scale : nullptr;
     sp.v_scale = fp8 ? kv->v_scale : nullptr;
     sp.status = dev->status;
-    {
-        ProfScope prof(PA_KERNEL_SPLIT_KV, s);
-        rc = launch_short(sp, maps.k, maps.v, D, fp8, short_grid, s);
-    }
-    if (rc != PA_OK) return fail(rc, "split-KV kernel launch failed: %s",
-                                 cudaGetErrorString(cudaGetLastError()));
 
-    if (!forbid_long) {
-        LongParams lp{};
+    // a long request has q_len * group > short_max_rows, so there are at
+    // most T / (short_max_rows / group + 1) of them
+    const int min_long_tokens = short_max_rows / group + 1;
+    const int max_long_reqs =
+        forbid_long ? 0 : std::min(num_seqs, T / std::max(1, min_long_tokens));
+    LongParams lp{};
+    int long_grid = 0;
+    if (max_long_reqs > 0) {
         lp.out = sp.out;
         lp.lse = lse;
         lp.out_f32 = nullptr;
@@ -406,18 +413,59 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
             lp.num_blocks = stg.cap;
             lp.kv_rows = stg.cap * kv->num_kv_heads * kv->block_size;
         }
+        long_grid = std::min(kv->num_kv_heads * ((T + tq - 1) / tq + max_long_reqs), L.max_long);
+    }
+    const CUtensorMap &lk = staged ? stg.tk : maps.k;
+    const CUtensorMap &lv = staged ? stg.tv : maps.v;
+
+    if (max_long_reqs > 0 && !profiling_active()) {
+        // The HBM-bound split-KV kernel and the tensor-core kernel run side by
+        // side: a first tensor-core grid takes part of the SMs (it waits
+        // for the plan, then lets the next grid in), the split-KV grid fills
+        // the others, and a second tensor-core grid takes SMs over as
+        // split-KV CTAs finish.  Both tensor-core grids pull items, longest
+        // first, from the step's counter; the second completes only after
+        // the first and after the split-KV grid.
+        LongParams l1 = lp;
+        l1.dynamic = 1;
+        l1.wait_start = 1;
+        l1.first_done = &hdr->first_done;
+        l1.first_ctas = -1;
+        // share of the SMs measured best on the mixed step: a third beside the
+        // HBM-bound bf16 split-KV kernel; a tenth beside the fp8 one, whose
+        // rate follows its SM count
+        const int g1 = std::min(std::max(1, fp8 ? dev->sms / 10 : dev->sms / 3), long_grid);
+        rc = launch_long(l1, maps.q, lk, lv, D, g1, s);
+        if (rc != PA_OK) return fail(rc, "tensor-core kernel launch failed: %s",
+                                     cudaGetErrorString(cudaGetLastError()));
+        sp.no_start_wait = 1;
+        rc = launch_short(sp, maps.k, maps.v, D, fp8, short_grid, s);
+        if (rc != PA_OK) return fail(rc, "split-KV kernel launch failed: %s",
+                                     cudaGetErrorString(cudaGetLastError()));
+        LongParams l2 = lp;
+        l2.dynamic = 1;
+        l2.overlap_prev = 1;
+        l2.first_done = &hdr->first_done;
+        l2.first_ctas = g1;
+        rc = launch_long(l2, maps.q, lk, lv, D, long_grid, s);
+        if (rc != PA_OK) return fail(rc, "tensor-core kernel launch failed: %s",
+                                     cudaGetErrorString(cudaGetLastError()));
+        return PA_OK;
+    }
+
+    {
+        ProfScope prof(PA_KERNEL_SPLIT_KV, s);
+        rc = launch_short(sp, maps.k, maps.v, D, fp8, short_grid, s);
+    }
+    if (rc != PA_OK) return fail(rc, "split-KV kernel launch failed: %s",
+                                 cudaGetErrorString(cudaGetLastError()));
+    if (max_long_reqs > 0) {
         // the split-KV kernel was launched just before: the tensor-core grid
         // may take over SMs as split-KV CTAs finish (its rows are disjoint)
         lp.overlap_prev = short_grid > 0 ? 1 : 0;
-        // a long request has q_len * group > short_max_rows, so there are at
-        // most T / (short_max_rows / group + 1) of them
-        const int min_long_tokens = short_max_rows / group + 1;
-        const int max_long_reqs = std::min(num_seqs, T / std::max(1, min_long_tokens));
-        const int grid = kv->num_kv_heads * ((T + tq - 1) / tq + max_long_reqs);
         {
             ProfScope prof(PA_KERNEL_TENSOR_CORE, s);
-            rc = launch_long(lp, maps.q, staged ? stg.tk : maps.k, staged ? stg.tv : maps.v, D,
-                             std::min(grid, L.max_long), s);
+            rc = launch_long(lp, maps.q, lk, lv, D, long_grid, s);
         }
         if (rc != PA_OK) return fail(rc, "tensor-core kernel launch failed: %s",
                                      cudaGetErrorString(cudaGetLastError()));

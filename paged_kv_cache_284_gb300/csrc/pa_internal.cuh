@@ -47,7 +47,8 @@ struct PlanHeader {
     int partial_rows;      // partial-state rows used
     int num_staged;        // fp8 pool: long requests given a bf16 staging copy
     int staged_blocks;     // staging blocks used
-    int pad[8];
+    int first_done;        // CTAs of the first tensor-core launch that finished
+    int pad[7];
 };
 static_assert(sizeof(PlanHeader) == 64, "header size");
 
@@ -122,6 +123,7 @@ struct ShortParams {
     float *partial_o, *partial_lse;
     const float *extra_o, *extra_lse;  // cascade: prefix state folded into the output
     const float *k_scale, *v_scale;    // fp8 pool: per-kv-head dequantisation scales
+    int no_start_wait;  // launched after the step's first tensor-core grid (see LongParams)
     unsigned *status;
 };
 
@@ -147,6 +149,16 @@ struct LongParams {
     // k_scale[h] and outputs by v_scale[h].  NULL for a bf16 pool.
     const int *stage_base;
     const float *k_scale, *v_scale;
+    // Step mode launch protocol.  dynamic: items from the step's counter
+    // (hdr->long_next) through a per-CTA queue, so several launches can share
+    // the work; wait_start: wait for the previous grid (the plan) before
+    // reading anything; first_done: completion counter of the step's first
+    // tensor-core launch -- that launch (first_ctas < 0) counts its CTAs,
+    // the last launch (first_ctas = the first launch's grid) completes only
+    // after all of them.
+    int dynamic, wait_start;
+    int *first_done;
+    int first_ctas;
     // 1: launched as a programmatic dependent of the split-KV kernel of the
     // same step.  The kernel then reads nothing but the plan's output (and
     // the step's inputs) before its last instruction, where it waits for the

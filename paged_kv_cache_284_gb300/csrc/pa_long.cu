@@ -57,8 +57,12 @@ struct LongGeom {
     // and partial sums [2 halves][128 rows]
     static constexpr int kOffXchg = kOffBar + kCtlBytes;
     static constexpr int kXchgBytes = (2 * 2 * 128 + 2 * 128) * 4;
+    // dynamic schedule: published item indices, their count, and how many
+    // each warp has read
+    static constexpr int kOffQueue = kOffXchg + kXchgBytes;
+    static constexpr int kQueueBytes = 512;
     // at least 116 KiB so that one CTA owns an SM (and its 512 TMEM columns)
-    static constexpr int kSmemRaw = kOffXchg + kXchgBytes + 1024;
+    static constexpr int kSmemRaw = kOffQueue + kQueueBytes + 1024;
     static constexpr int kSmemBytes = kSmemRaw > 116 * 1024 ? kSmemRaw : 116 * 1024;
     // TMEM columns: S0 | S1 (fp32 scores) | O (fp32) | P0 | P1 (bf16 pairs)
     static constexpr uint32_t kTmemCols = 512;
@@ -176,6 +180,66 @@ __device__ __forceinline__ int serpentine_item(int round) {
     return round * g + ((round & 1) ? g - 1 - c : c);
 }
 
+// Dynamic schedule (p.dynamic): warp 0 -- the K producer, which runs ahead
+// of every other role -- takes item indices from the step's counter, shared
+// by every launch of the step, and publishes them in order in a shared
+// memory queue; every other warp reads them back in the same order.  A
+// CTA that starts late therefore simply takes fewer items.
+constexpr int kItemQueue = 64;
+constexpr int kSchedDone = -1, kSchedAbort = -2;
+struct Sched {
+    int *idx;            // [kItemQueue]
+    volatile int *pub;   // items published
+    volatile int *cons;  // [kLongWarps] items read per warp
+};
+
+__device__ __forceinline__ bool sched_spin(bool (*ready)(const Sched &, int), const Sched &sc,
+                                           int k, volatile int *abort) {
+    if (ready(sc, k)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (ready(sc, k)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+__device__ bool sched_published(const Sched &sc, int k) { return *sc.pub > k; }
+__device__ bool sched_slot_free(const Sched &sc, int k) {
+    for (int w = 1; w < kLongWarps; ++w)
+        if (sc.cons[w] <= k - kItemQueue) return false;
+    return true;
+}
+
+// Item of round k of this role, or kSchedDone / kSchedAbort.  One thread of
+// the warp calls it (a whole-warp role broadcasts the result).
+__device__ __forceinline__ int sched_take(const LongParams &p, const Sched &sc, int n_items,
+                                          int k, int warp, volatile int *abort) {
+    if (!p.dynamic) {
+        if (k * static_cast<int>(gridDim.x) >= n_items) return kSchedDone;
+        const int idx = serpentine_item(k);
+        return idx < n_items ? idx : kSchedDone;
+    }
+    const int slot = k % kItemQueue;
+    int idx;
+    if (warp == 0) {
+        if (k >= kItemQueue && !sched_spin(sched_slot_free, sc, k, abort)) return kSchedAbort;
+        idx = atomicAdd(&p.hdr->long_next, 1);
+        if (idx >= n_items) idx = kSchedDone;
+        sc.idx[slot] = idx;
+        __threadfence_block();
+        *sc.pub = k + 1;
+    } else {
+        if (!sched_spin(sched_published, sc, k, abort)) return kSchedAbort;
+        __threadfence_block();
+        idx = reinterpret_cast<volatile int *>(sc.idx)[slot];
+        sc.cons[warp] = k + 1;
+    }
+    return idx;
+}
+
 __device__ __forceinline__ int num_items(const LongParams &p) {
     if (p.prefix_mode) return p.num_kv_heads * p.prefix_q_tiles * p.prefix_nsplit;
     return *reinterpret_cast<volatile int *>(&p.hdr->num_long_items);
@@ -184,18 +248,25 @@ __device__ __forceinline__ int num_items(const LongParams &p) {
 // Producer loop shared by the K warp (0, which also loads Q) and the V warp
 // (6): gathers one 128-key tile per step into its ring.
 template <int D, int NS>
-__device__ void produce(const LongParams &p, const CUtensorMap *tm, uint8_t *ring,
+__device__ void produce(const LongParams &p, const Sched &sc, const CUtensorMap *tm, uint8_t *ring,
                         uint64_t *full, uint64_t *empty, Bars *bars, bool load_q,
                         const CUtensorMap *tmq, uint8_t *sQ, volatile int *abort_flag) {
     using G = LongGeom<D>;
     const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const int n_items = num_items(p);
     uint32_t t = 0;        // tiles issued by this warp so far (all items)
     uint32_t k_item = 0;   // items (with keys) started so far
     bool ok = true;
-    for (int round = 0; ok && round * static_cast<int>(gridDim.x) < n_items; ++round) {
-        const int idx = serpentine_item(round);
-        if (idx >= n_items) continue;
+    for (int round = 0; ok; ++round) {
+        int idx = 0;
+        if (lane == 0) idx = sched_take(p, sc, n_items, round, warp, abort_flag);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        if (idx == kSchedDone) break;
+        if (idx == kSchedAbort) {
+            ok = false;
+            break;
+        }
         const Item it = decode_item(p, idx);
         if (it.nt == 0) continue;
         if (load_q) {
@@ -274,11 +345,20 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctl + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (p.wait_start) {
+        pdl_wait();     // the plan (and any staging copy) first
+        pdl_trigger();  // then the split-KV grid may take the other SMs
+    }
     const int n_items = num_items(p);
-    if (static_cast<int>(blockIdx.x) >= n_items) {
+    if (!p.dynamic && static_cast<int>(blockIdx.x) >= n_items) {
         pdl_wait();  // complete only after the grid this one overlaps
         return;
     }
+    int *qmem = reinterpret_cast<int *>(smem + G::kOffQueue);
+    Sched sched;
+    sched.idx = qmem;
+    sched.pub = qmem + kItemQueue;
+    sched.cons = qmem + kItemQueue + 1;
 
     // ---- setup ----------------------------------------------------------------
     if (threadIdx.x == 0) {
@@ -307,6 +387,8 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
         mbar_init(&bars->drain_pv, 1);
         ctl[0] = 0;
         ctl[1] = 0;
+        *sched.pub = 0;
+        for (int w = 0; w < kLongWarps; ++w) sched.cons[w] = 0;
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, G::kTmemCols);
@@ -325,12 +407,12 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
             tma_prefetch_desc(&tmq);
             tma_prefetch_desc(&tmk);
         }
-        produce<D, kKStages>(p, &tmk, sK, bars->k_full, bars->k_empty, bars, true, &tmq, sQ,
+        produce<D, kKStages>(p, sched, &tmk, sK, bars->k_full, bars->k_empty, bars, true, &tmq, sQ,
                              abort_flag);
     } else if (warp == kWarpV) {
         // ============================ V loads ============================
         if (lane == 0) tma_prefetch_desc(&tmv);
-        produce<D, kVStages>(p, &tmv, sV, bars->v_full, bars->v_empty, bars, false, nullptr,
+        produce<D, kVStages>(p, sched, &tmv, sV, bars->v_full, bars->v_empty, bars, false, nullptr,
                              nullptr, abort_flag);
     } else if (warp == 1) {
         // ============================ Q K^T issuer ============================
@@ -341,9 +423,13 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
             const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK);
             uint32_t t = 0, k_item = 0;
             bool ok = true;
-            for (int round = 0; ok && round * static_cast<int>(gridDim.x) < n_items; ++round) {
-        const int idx = serpentine_item(round);
-        if (idx >= n_items) continue;
+            for (int round = 0; ok; ++round) {
+                const int idx = sched_take(p, sched, n_items, round, warp, abort_flag);
+                if (idx == kSchedDone) break;
+                if (idx == kSchedAbort) {
+                    ok = false;
+                    break;
+                }
                 const Item it = decode_item(p, idx);
                 if (it.nt == 0) continue;
                 if (!mbar_wait(&bars->q_full, k_item & 1, abort_flag)) { ok = false; break; }
@@ -388,9 +474,13 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
             const uint32_t v_addr = smem_u32(sV);
             uint32_t t = 0, k_item = 0;
             bool ok = true;
-            for (int round = 0; ok && round * static_cast<int>(gridDim.x) < n_items; ++round) {
-        const int idx = serpentine_item(round);
-        if (idx >= n_items) continue;
+            for (int round = 0; ok; ++round) {
+                const int idx = sched_take(p, sched, n_items, round, warp, abort_flag);
+                if (idx == kSchedDone) break;
+                if (idx == kSchedAbort) {
+                    ok = false;
+                    break;
+                }
                 const Item it = decode_item(p, idx);
                 if (it.nt == 0) continue;
                 for (int j = 0; j < it.nt; ++j) {
@@ -451,9 +541,15 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
             theirs = slots[(1 - half) * 128 + r];
             return w;
         };
-        for (int round = 0; ok && round * static_cast<int>(gridDim.x) < n_items; ++round) {
-        const int idx = serpentine_item(round);
-        if (idx >= n_items) continue;
+        for (int round = 0; ok; ++round) {
+            int idx = 0;
+            if (lane == 0) idx = sched_take(p, sched, n_items, round, warp, abort_flag);
+            idx = __shfl_sync(0xffffffffu, idx, 0);
+            if (idx == kSchedDone) break;
+            if (idx == kSchedAbort) {
+                ok = false;
+                break;
+            }
             const Item it = decode_item(p, idx);
             const bool row_valid = ttok < it.nvalid && r < p.q_tile_tokens * p.group;
             const int row_limit = it.causal ? it.pos0 + ttok : 0x7fffffff;
@@ -714,6 +810,23 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
     // with overlap_prev: this grid completes only after the split-KV grid it
     // overlapped, so later work on the stream is still ordered after both
     pdl_wait();
+    if (p.first_done && threadIdx.x == 0) {
+        if (p.first_ctas < 0) {
+            // a first launch of the step: count this CTA done (its outputs first)
+            __threadfence();
+            atomicAdd(p.first_done, 1);
+        } else {
+            // the last launch: complete only after every CTA of the first one
+            const uint64_t t0 = global_timer_ns();
+            while (*reinterpret_cast<volatile int *>(p.first_done) < p.first_ctas) {
+                if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+                    flag_status(p.status, PA_DEV_WAIT_TIMEOUT);
+                    break;
+                }
+            }
+            __threadfence();
+        }
+    }
 }
 
 size_t long_smem_bytes(int head_dim) {
@@ -742,7 +855,7 @@ int launch_long(const LongParams &p, const CUtensorMap &tq, const CUtensorMap &t
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return PA_ERR_CUDA;
     grid = grid < sms ? grid : sms;
-    const bool pdl = p.overlap_prev != 0;
+    const bool pdl = p.overlap_prev != 0 || p.wait_start != 0;
     if (head_dim == 128) {
         if (configure_long<128>() != PA_OK) return PA_ERR_CUDA;
         PdlLaunch l(grid, 32 * kLongWarps, LongGeom<128>::kSmemBytes, s, pdl);

@@ -345,6 +345,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         p.hdr->split_stages = sp;
         p.hdr->partial_rows = row_base;
         p.hdr->num_staged = s_overflow ? 0 : staged;
+        p.hdr->first_done = 0;
         p.hdr->staged_blocks = s_overflow ? 0 : staged_blocks;
     }
 }

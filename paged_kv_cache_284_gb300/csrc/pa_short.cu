@@ -398,8 +398,9 @@ __global__ void __launch_bounds__(kShortThreads, 2)
         tma_prefetch_desc(&tmv);
     }
     __syncthreads();
-    // everything below reads the plan's output
-    pdl_wait();
+    // everything below reads the plan's output; after the step's first
+    // tensor-core grid (which waited for the plan) there is nothing to wait for
+    if (!p.no_start_wait) pdl_wait();
     pdl_trigger();
 
     auto k_box = [&](int slot, int c, int hf) -> uint8_t * {
