@@ -280,9 +280,12 @@ const char *pa_status_string(int code);
  * Profiling hook.  After this call, every launch of kernel `which` made by
  * the calls above is bracketed by cudaEventRecord(start_event) and
  * cudaEventRecord(end_event) on the launch stream, so a caller can time one
- * kernel of a step with events (the step itself is unchanged).  Events are
- * cudaEvent_t passed as void*; NULL clears the hook.  The setting is
- * process-wide; set it from one thread at a time.
+ * kernel of a step with events.  While events are set for the split-KV or
+ * the tensor-core kernel, pa_attention launches those two one after the
+ * other (one tensor-core grid) instead of side by side; the results are
+ * the same bit for bit.  Events are cudaEvent_t passed as void*; NULL
+ * clears the hook.  The setting is process-wide; set it from one thread at
+ * a time.
  *   which: PA_KERNEL_WRITE_KV, PA_KERNEL_PLAN, PA_KERNEL_SPLIT_KV,
  *          PA_KERNEL_TENSOR_CORE
  */
@@ -295,6 +298,14 @@ int pa_set_profile_events(int32_t which, void *start_event, void *end_event);
  * device.  Synchronises `stream` first.  HOST pointer `status`.
  */
 int pa_read_device_status(uint32_t *status, int clear, void *stream);
+
+/*
+ * Number of kernels the library has enqueued in this process since it was
+ * loaded, on any stream or device (launches recorded into a CUDA graph
+ * count once, when captured; replays do not count).  Read it before and
+ * after a region of calls to count their launches.  Thread-safe.
+ */
+uint64_t pa_kernel_launches(void);
 
 #ifdef __cplusplus
 }

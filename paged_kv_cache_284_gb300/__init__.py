@@ -35,7 +35,7 @@ EXPORTED = ["pa_write_kv", "pa_attention_workspace_size", "pa_attention", "pa_at
             "pa_merge_states", "pa_cascade_workspace_size", "pa_prefix_attention",
             "pa_cascade_decode", "pa_validate_metadata", "pa_last_error_message",
             "pa_status_string", "pa_read_device_status", "pa_set_profile_events",
-            "pa_attention_no_alloc", "pa_fp8_staging_bytes",
+            "pa_attention_no_alloc", "pa_fp8_staging_bytes", "pa_kernel_launches",
             # block manager (include/pa_blocks.h)
             "pa_bm_create", "pa_bm_destroy", "pa_bm_add_request", "pa_bm_append_tokens",
             "pa_bm_fork", "pa_bm_schedule", "pa_bm_free_request", "pa_bm_num_free_blocks",
@@ -90,6 +90,7 @@ def _declare(lib):
         "pa_attention_no_alloc": ([P, KV, P, i32, P, P, P, i32, i32, i32, f32, P, P, P],
                                   ctypes.c_int),
         "pa_fp8_staging_bytes": ([i32, i32, i32, i64], sz),
+        "pa_kernel_launches": ([], ctypes.c_uint64),
         "pa_bm_create": ([i32, i32], P),
         "pa_bm_destroy": ([P], None),
         "pa_bm_add_request": ([P, i64, P, i32, P], ctypes.c_int),
@@ -317,6 +318,11 @@ def read_device_status(clear: bool = True, stream=None) -> int:
     _check(lib().pa_read_device_status(ctypes.byref(v), 1 if clear else 0, _stream(stream)),
            "pa_read_device_status")
     return int(v.value)
+
+
+def kernel_launches() -> int:
+    """Kernels the library has enqueued in this process so far."""
+    return int(lib().pa_kernel_launches())
 
 
 def set_profile_events(which: int, start=None, end=None):

@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstring>
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -114,6 +115,8 @@ int make_q_map(CUtensorMap *m, const void *q, int tokens, int heads, int head_di
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : fail(PA_ERR_CUDA, "Q tensor map encode failed (%d)", (int)r);
 }
+
+std::atomic<unsigned long long> g_launches{0};
 
 // Profiling hook state (pa_set_profile_events).
 void *g_prof[4][2] = {};
@@ -326,6 +329,7 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
     pp.split_stages = split_keys / kStageKeys;
     const int short_grid = dev->sms * dev->short_ctas_per_sm[fp8 ? 2 : (D == 128 ? 1 : 0)];
     pp.target_items = kSplitItemsPerCta * short_grid;
+    pp.num_ctas = short_grid;
     pp.hdr = hdr;
     pp.short_items = reinterpret_cast<ShortItem *>(ws + L.short_items);
     pp.long_items = reinterpret_cast<LongItem *>(ws + L.long_items);
@@ -560,6 +564,8 @@ int prefix_partial_rows(int T, int prefix_len, int num_kv_heads, int group) {
 }  // namespace
 
 namespace pa {
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 // Attention for one step inside a caller-provided scratch region of fixed
 // size (used by the entry point that never allocates).  The work lists get
@@ -898,5 +904,7 @@ int pa_read_device_status(uint32_t *status, int clear, void *stream) {
     }
     return PA_OK;
 }
+
+uint64_t pa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

@@ -11,6 +11,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/pa.h"
 
 namespace pa {
@@ -65,7 +67,7 @@ static_assert(sizeof(PlanHeader) == 64, "header size");
 struct alignas(16) ShortItem {
     int b, split, nsplit, stage_begin;
     int stage_end, partial_base, q_begin, q_count;
-    int counter, pad0, pad1, pad2;
+    int counter, seq_len, pad1, pad2;  // seq_len: the request's, read once by the plan
 };
 static_assert(sizeof(ShortItem) == 48, "item size");
 
@@ -179,6 +181,7 @@ struct PlanParams {
     int *stage_base, *stage_list;
     int split_stages;    // 0 = automatic
     int target_items;    // automatic split aims at about this many split-KV items
+    int num_ctas;        // persistent split-KV CTAs of the launch
     PlanHeader *hdr;
     ShortItem *short_items;
     LongItem *long_items;
@@ -207,6 +210,16 @@ struct PdlLaunch {
     PdlLaunch(const PdlLaunch &) = delete;
     PdlLaunch &operator=(const PdlLaunch &) = delete;
 };
+
+// Every kernel launch of the library goes through launch_kernel, which keeps
+// the process-wide count that pa_kernel_launches() reports.
+void count_launch();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(const PdlLaunch &l, void (*kernel)(KArgs...), Args &&...args) {
+    const cudaError_t e = cudaLaunchKernelEx(&l.cfg, kernel, std::forward<Args>(args)...);
+    if (e == cudaSuccess) count_launch();
+    return e;
+}
 
 // Host-side launchers (each defined next to its kernel).
 int launch_write_kv(const void *k, const void *v, const int64_t *slots, int num_tokens,
@@ -250,6 +263,19 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// Atomic add at GPU scope with acquire-release semantics.  It publishes the
+// writes ordered before it (the CTA's, through a preceding CTA barrier) and,
+// to the thread that reads the final count, makes visible what the other
+// adders published.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *ptr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(ptr), "r"(v)
+                 : "memory");
+    return old;
 }
 
 __device__ __forceinline__ void flag_status(unsigned *status, unsigned bits) {

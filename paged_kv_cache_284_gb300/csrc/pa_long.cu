@@ -859,13 +859,13 @@ int launch_long(const LongParams &p, const CUtensorMap &tq, const CUtensorMap &t
     if (head_dim == 128) {
         if (configure_long<128>() != PA_OK) return PA_ERR_CUDA;
         PdlLaunch l(grid, 32 * kLongWarps, LongGeom<128>::kSmemBytes, s, pdl);
-        return cudaLaunchKernelEx(&l.cfg, long_kernel<128>, p, tq, tk, tv) == cudaSuccess
+        return launch_kernel(l, long_kernel<128>, p, tq, tk, tv) == cudaSuccess
                    ? PA_OK
                    : PA_ERR_CUDA;
     }
     if (configure_long<64>() != PA_OK) return PA_ERR_CUDA;
     PdlLaunch l(grid, 32 * kLongWarps, LongGeom<64>::kSmemBytes, s, pdl);
-    return cudaLaunchKernelEx(&l.cfg, long_kernel<64>, p, tq, tk, tv) == cudaSuccess ? PA_OK
+    return launch_kernel(l, long_kernel<64>, p, tq, tk, tv) == cudaSuccess ? PA_OK
                                                                                     : PA_ERR_CUDA;
 }
 

@@ -49,10 +49,12 @@ int launch_merge(const void *oa, const float *la, const void *ob, const float *l
     const int pieces = head_dim / 8;
     const int64_t total = rows * pieces;
     const int threads = 256;
-    merge_states_kernel<<<static_cast<unsigned>((total + threads - 1) / threads), threads, 0, s>>>(
-        static_cast<const uint4 *>(oa), la, static_cast<const uint4 *>(ob), lb, rows, pieces,
-        static_cast<uint4 *>(out), lse_out);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    PdlLaunch l(static_cast<unsigned>((total + threads - 1) / threads), threads, 0, s, false);
+    return launch_kernel(l, merge_states_kernel, static_cast<const uint4 *>(oa), la,
+                         static_cast<const uint4 *>(ob), lb, rows, pieces,
+                         static_cast<uint4 *>(out), lse_out) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 
 }  // namespace pa

@@ -44,22 +44,102 @@ __device__ int block_exclusive_scan(int v, int *tmp, int *total) {
     return res;
 }
 
-__device__ long long block_sum_ll(long long v, long long *tmp) {
+// Exact warp sum of non-negative 64-bit values with single-instruction warp
+// reductions: three slices of 21, 21 and 22 bits are summed separately (32
+// lanes x 2^22 < 2^32, so no slice overflows) and recombined.
+__device__ __forceinline__ long long warp_sum_ll(long long x) {
+    const unsigned long long v = static_cast<unsigned long long>(x);
+    const unsigned a = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(v & 0x1fffffu));
+    const unsigned b = __reduce_add_sync(0xffffffffu, static_cast<unsigned>((v >> 21) & 0x1fffffu));
+    const unsigned c = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(v >> 42));
+    return static_cast<long long>(a + (static_cast<unsigned long long>(b) << 21) +
+                                  (static_cast<unsigned long long>(c) << 42));
+}
+
+// Block-wide sums of N non-negative 64-bit values and the maximum of one
+// non-negative int, all in one pass (two barriers for the lot).
+constexpr int kRedStride = kPlanThreads / 32 + 1;
+template <int N>
+__device__ void block_reduce(long long (&v)[N], int &mx, long long *tmp) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) tmp[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-        long long w = (lane < (kPlanThreads / 32)) ? tmp[lane] : 0;
+    for (int i = 0; i < N; ++i) v[i] = warp_sum_ll(v[i]);
+    mx = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(mx)));
+    if (lane == 0) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
-        if (lane == 0) tmp[32] = w;
+        for (int i = 0; i < N; ++i) tmp[i * kRedStride + warp] = v[i];
+        tmp[N * kRedStride + warp] = mx;
     }
     __syncthreads();
-    const long long r = tmp[32];
+    if (warp == 0) {
+        const bool in = lane < kPlanThreads / 32;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const long long w = warp_sum_ll(in ? tmp[i * kRedStride + lane] : 0);
+            if (lane == 0) tmp[i * kRedStride + 32] = w;
+        }
+        const unsigned m = __reduce_max_sync(
+            0xffffffffu, in ? static_cast<unsigned>(tmp[N * kRedStride + lane]) : 0u);
+        if (lane == 0) tmp[N * kRedStride + 32] = m;
+    }
     __syncthreads();
-    return r;
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = tmp[i * kRedStride + 32];
+    mx = static_cast<int>(tmp[N * kRedStride + 32]);
+    __syncthreads();
+}
+
+// Exclusive block-wide prefix sums of two values at once (tmp: 66 ints).
+__device__ void block_exclusive_scan2(int a, int b, int *tmp, int &pa, int &pb, int &ta, int &tb) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int ia = a, ib = b;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int na = __shfl_up_sync(0xffffffffu, ia, o);
+        const int nb = __shfl_up_sync(0xffffffffu, ib, o);
+        if (lane >= o) {
+            ia += na;
+            ib += nb;
+        }
+    }
+    if (lane == 31) {
+        tmp[warp] = ia;
+        tmp[33 + warp] = ib;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const bool in = lane < kPlanThreads / 32;
+        const int wa = in ? tmp[lane] : 0, wb = in ? tmp[33 + lane] : 0;
+        int sa = wa, sb = wb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int na = __shfl_up_sync(0xffffffffu, sa, o);
+            const int nb = __shfl_up_sync(0xffffffffu, sb, o);
+            if (lane >= o) {
+                sa += na;
+                sb += nb;
+            }
+        }
+        tmp[lane] = sa - wa;
+        tmp[33 + lane] = sb - wb;
+        if (lane == 31) {
+            tmp[32] = sa;
+            tmp[65] = sb;
+        }
+    }
+    __syncthreads();
+    pa = tmp[warp] + ia - a;
+    pb = tmp[33 + warp] + ib - b;
+    ta = tmp[32];
+    tb = tmp[65];
+    __syncthreads();
+}
+
+__device__ long long block_sum_ll(long long v, long long *tmp) {
+    long long a[1] = {v};
+    int m = 0;
+    block_reduce<1>(a, m, tmp);
+    return a[0];
 }
 
 struct ReqInfo {
@@ -122,25 +202,30 @@ __device__ __forceinline__ int short_bin(int stages) {
     return kSortBins - 1 - min(stages, kSortBins - 1);
 }
 
-// First stage of split s of ns over `stages` stages (s = ns gives the end).
-__device__ __forceinline__ int split_begin(int stages, int ns, int s) {
-    return static_cast<int>(static_cast<long long>(stages) * s / ns);
+// A piece of `stages` stages cut into ns splits whose ranges differ by at
+// most one stage: the first `rem` splits take q + 1 stages, the others q.
+struct SplitCut {
+    int ns, q, rem;
+};
+__device__ __forceinline__ SplitCut split_cut(int stages, int sp) {
+    SplitCut c;
+    c.ns = (stages + sp - 1) / sp;
+    c.q = stages / c.ns;
+    c.rem = stages - c.q * c.ns;
+    return c;
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
-    __shared__ int tmp[33];
-    __shared__ long long tmpl[33];
+    __shared__ int tmp[66];
+    __shared__ long long tmpl[5 * kRedStride];
     __shared__ int bins[kSortBins];
-    __shared__ int s_split, s_overflow, s_max_stages;
-    const int tid = threadIdx.x, lane = tid & 31;
+    __shared__ int s_overflow;
+    const int tid = threadIdx.x;
     const int hkv = p.num_kv_heads;
     // the metadata (and the workspace) may belong to the previous kernel
     pdl_wait();
     pdl_trigger();
-    if (tid == 0) {
-        s_overflow = 0;
-        s_max_stages = 0;
-    }
+    if (tid == 0) s_overflow = 0;
     for (int i = tid; i < kSortBins; i += kPlanThreads) bins[i] = 0;
     // 0. fp8 pool with a staging area: long requests get consecutive bf16
     // staging blocks in request order while they fit (a request that does
@@ -174,70 +259,103 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     auto req = [&](int b) { return b == tid ? mine : load_req(p, b); };
     __syncthreads();
 
-    // 1. total split-KV work (in stages) -------------------------------------
-    long long work = 0;
-    int max_stages = 0, pieces = 0;
+    // 1. totals: split-KV work (in stages), pieces, longest piece, query tiles
+    long long tot[3] = {0, 0, 0};  // work, pieces, tensor-core query tiles
+    int max_stages = 0;
     for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
         const ReqInfo r = req(b);
         for (int i = 0; i < r.pieces; ++i) {
             const Piece pc = piece_of(p, r, i);
-            work += pc.stages;
+            tot[0] += pc.stages;
             max_stages = max(max_stages, pc.stages);
         }
-        pieces += r.pieces;
+        tot[1] += r.pieces;
+        tot[2] += r.qtiles;
     }
-    max_stages = __reduce_max_sync(0xffffffffu, max_stages);
-    if (lane == 0 && max_stages > 0) atomicMax(&s_max_stages, max_stages);
-    const long long total_work = block_sum_ll(work, tmpl) * hkv;  // also orders the atomics
-    const long long total_pieces = block_sum_ll(pieces, tmpl);
+    block_reduce<3>(tot, max_stages, tmpl);
+    const long long total_work = tot[0] * hkv;
+    const long long total_pieces = tot[1];
+    const long long total_qtiles = tot[2];
 
     // 2. split size ------------------------------------------------------------
-    int sp;
+    // A split-KV item costs its stages plus a fixed cost (first-data latency
+    // and the split epilogue) worth a few stages.  When every piece can have
+    // a CTA of its own (P <= C items unsplit), the cut aims at one item per
+    // CTA, so that all items run in a single round: sum_i ceil(s_i / sp) <=
+    // W / sp + P, so sp = W / (C - P) always fits, and W / (C - P / 2) (half
+    // an item of rounding per piece) usually does and gives shorter items.
+    // Otherwise items aim at about target_items, so that longest-first
+    // dynamic scheduling balances the CTAs.  One counting pass checks both
+    // candidates and the work-list capacities; the doubling loop below runs
+    // only if they overflow.  (32-bit arithmetic: W saturates, which only
+    // coarsens the heuristic.)
+    const int W = static_cast<int>(min(total_work, 1LL << 30));
+    const int P = static_cast<int>(min(total_pieces * hkv, 1LL << 30));
+    const int C = max(1, p.num_ctas);
+    int sp_a = kMinSplitStages, sp_b = kMinSplitStages;
     if (p.split_stages > 0) {
-        sp = p.split_stages;
-    } else {
-        const long long tgt = max(1, p.target_items);
-        sp = static_cast<int>(max(static_cast<long long>(kMinSplitStages),
-                                  (total_work + tgt - 1) / tgt));
+        sp_a = sp_b = p.split_stages;
+    } else if (W > 0 && P <= C) {
+        const int da = C - P / 2;
+        sp_a = max(kMinSplitStages, (W + da - 1) / da);
+        sp_b = P < C ? max(kMinSplitStages, (W + (C - P) - 1) / (C - P)) : max(sp_a, max_stages);
+    } else if (W > 0) {
+        const int tgt = max(1, p.target_items);
+        sp_a = sp_b = max(kMinSplitStages, (W + tgt - 1) / tgt);
     }
+    long long cnt[4] = {0, 0, 0, 0};  // items and partial-state rows at sp_a, at sp_b
+    for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+        const ReqInfo r = req(b);
+        for (int i = 0; i < r.pieces; ++i) {
+            const Piece pc = piece_of(p, r, i);
+            const int na = (pc.stages + sp_a - 1) / sp_a, nb = (pc.stages + sp_b - 1) / sp_b;
+            cnt[0] += na;
+            cnt[2] += nb;
+            if (na > 1) cnt[1] += static_cast<long long>(na) * pc.q_count * p.group;
+            if (nb > 1) cnt[3] += static_cast<long long>(nb) * pc.q_count * p.group;
+        }
+    }
+    {
+        int unused = 0;
+        block_reduce<4>(cnt, unused, tmpl);
+    }
+    const bool one_round = p.split_stages <= 0 && W > 0 && P <= C;
+    const bool use_a = !one_round || cnt[0] * hkv <= C;
+    int sp = use_a ? sp_a : sp_b;
+    long long items = (use_a ? cnt[0] : cnt[2]) * hkv, rows = (use_a ? cnt[1] : cnt[3]) * hkv;
     for (int guard = 0; guard < 40; ++guard) {
-        long long items = 0, rows = 0;
+        if ((items <= p.max_short && rows <= p.cap_rows) || sp >= max_stages) break;
+        sp *= 2;
+        long long c2[2] = {0, 0};
         for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
             const ReqInfo r = req(b);
             for (int i = 0; i < r.pieces; ++i) {
                 const Piece pc = piece_of(p, r, i);
                 const int ns = (pc.stages + sp - 1) / sp;
-                items += ns;
-                if (ns > 1) rows += static_cast<long long>(ns) * pc.q_count * p.group;
+                c2[0] += ns;
+                if (ns > 1) c2[1] += static_cast<long long>(ns) * pc.q_count * p.group;
             }
         }
-        items = block_sum_ll(items, tmpl) * hkv;
-        rows = block_sum_ll(rows, tmpl) * hkv;
-        if ((items <= p.max_short && rows <= p.cap_rows) || sp >= s_max_stages) break;
-        sp *= 2;
+        int unused = 0;
+        block_reduce<2>(c2, unused, tmpl);
+        items = c2[0] * hkv;
+        rows = c2[1] * hkv;
     }
-    if (tid == 0) {
-        s_split = sp;
-        if (total_pieces * hkv > p.num_counters) s_overflow = 1;
-    }
-    __syncthreads();
-    sp = s_split;
+    if (tid == 0 && total_pieces * hkv > p.num_counters) s_overflow = 1;
 
     int short_base = 0, long_base = 0, row_base = 0, piece_base = 0;
 
     // 3. split-KV items, longest key range first (counting sort on the number
-    // of stages of the item).  A piece's ns splits cut its stages into ranges
-    // that differ by at most one stage.  Partial-state rows and completion
-    // counters are handed out in request order by block scans.
+    // of stages of the item).  A piece's splits of equal length take
+    // consecutive slots of their bin, reserved with one atomic.  Partial-state
+    // rows and completion counters are handed out in request order by block
+    // scans.
     for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
         const ReqInfo r = req(b);
         for (int i = 0; i < r.pieces; ++i) {
-            const Piece pc = piece_of(p, r, i);
-            const int ns = (pc.stages + sp - 1) / sp;
-            for (int s = 0; s < ns; ++s)
-                atomicAdd(&bins[short_bin(split_begin(pc.stages, ns, s + 1) -
-                                          split_begin(pc.stages, ns, s))],
-                          1);
+            const SplitCut c = split_cut(piece_of(p, r, i).stages, sp);
+            if (c.rem > 0) atomicAdd(&bins[short_bin(c.q + 1)], c.rem);
+            if (c.ns > c.rem) atomicAdd(&bins[short_bin(c.q)], c.ns - c.rem);
         }
     }
     __syncthreads();
@@ -259,9 +377,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
             const int ns = (pc.stages + sp - 1) / sp;
             if (ns > 1) n_rows += ns * pc.q_count * p.group * hkv;
         }
-        int tot_r, tot_p;
-        const int off_r = row_base + block_exclusive_scan(n_rows, tmp, &tot_r);
-        const int off_p = piece_base + block_exclusive_scan(r.pieces, tmp, &tot_p);
+        int off_r, off_p, tot_r, tot_p;
+        block_exclusive_scan2(n_rows, r.pieces, tmp, off_r, off_p, tot_r, tot_p);
+        off_r += row_base;
+        off_p += piece_base;
         row_base += tot_r;
         piece_base += tot_p;
         if (static_cast<long long>(short_base) * hkv > p.max_short || row_base > p.cap_rows ||
@@ -272,25 +391,27 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         int row = off_r;
         for (int i = 0; i < r.pieces; ++i) {
             const Piece pc = piece_of(p, r, i);
-            const int ns = (pc.stages + sp - 1) / sp;
+            const SplitCut c = split_cut(pc.stages, sp);
             const int R = pc.q_count * p.group;
-            for (int s = 0; s < ns; ++s) {
-                const int s0 = split_begin(pc.stages, ns, s);
-                const int s1 = split_begin(pc.stages, ns, s + 1);
-                ShortItem it;
-                it.b = b;
+            const int slot_hi = c.rem > 0 ? atomicAdd(&bins[short_bin(c.q + 1)], c.rem) : 0;
+            const int slot_lo = c.ns > c.rem ? atomicAdd(&bins[short_bin(c.q)], c.ns - c.rem) : 0;
+            ShortItem it;
+            it.b = b;
+            it.nsplit = c.ns;
+            it.q_begin = pc.q_begin;
+            it.q_count = pc.q_count;
+            it.counter = off_p + i;
+            it.seq_len = r.len;
+            it.pad1 = it.pad2 = 0;
+            for (int s = 0; s < c.ns; ++s) {
+                const bool big = s < c.rem;
                 it.split = s;
-                it.nsplit = ns;
-                it.stage_begin = s0;
-                it.stage_end = s1;
-                it.partial_base = (ns > 1) ? row + s * R : 0;
-                it.q_begin = pc.q_begin;
-                it.q_count = pc.q_count;
-                it.counter = off_p + i;
-                it.pad0 = it.pad1 = it.pad2 = 0;
-                store_record(p.short_items, atomicAdd(&bins[short_bin(s1 - s0)], 1), it);
+                it.stage_begin = s * c.q + min(s, c.rem);
+                it.stage_end = it.stage_begin + c.q + (big ? 1 : 0);
+                it.partial_base = (c.ns > 1) ? row + s * R : 0;
+                store_record(p.short_items, big ? slot_hi + s : slot_lo + (s - c.rem), it);
             }
-            if (ns > 1) row += ns * R * hkv;
+            if (c.ns > 1) row += c.ns * R * hkv;
         }
     }
     __syncthreads();
@@ -298,36 +419,38 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     // 3b. tensor-core items, longest key range first (counting sort on the
     // number of 128-key tiles), so persistent CTAs that take items in order
     // finish together.
-    for (int i = tid; i < kSortBins; i += kPlanThreads) bins[i] = 0;
-    __syncthreads();
-    for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
-        const ReqInfo r = req(b);
-        for (int qt = 0; qt < r.qtiles; ++qt)
-            atomicAdd(&bins[long_bin(p, r, qt)], 1);
-    }
-    __syncthreads();
-    {
-        // one bin per thread: exclusive scan gives each bin's first slot
-        int tot_l;
-        const int v = tid < kSortBins ? bins[tid] : 0;
-        const int off = block_exclusive_scan(v, tmp, &tot_l);
-        if (tid < kSortBins) bins[tid] = off;
-        long_base = tot_l;
+    if (total_qtiles > 0) {
+        for (int i = tid; i < kSortBins; i += kPlanThreads) bins[i] = 0;
         __syncthreads();
-    }
-    if (static_cast<long long>(long_base) * hkv > p.max_long) {
-        if (tid == 0) s_overflow = 1;
-    } else {
         for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
             const ReqInfo r = req(b);
-            for (int qt = 0; qt < r.qtiles; ++qt) {
-                const int nvalid = min(p.q_tile_tokens, r.n - qt * p.q_tile_tokens);
-                LongItem it{};
-                it.b = b;
-                it.q_tile = qt;
-                it.key_begin = 0;
-                it.key_end = min(r.len, r.ctx + qt * p.q_tile_tokens + nvalid);
-                store_record(p.long_items, atomicAdd(&bins[long_bin(p, r, qt)], 1), it);
+            for (int qt = 0; qt < r.qtiles; ++qt)
+                atomicAdd(&bins[long_bin(p, r, qt)], 1);
+        }
+        __syncthreads();
+        {
+            // one bin per thread: exclusive scan gives each bin's first slot
+            int tot_l;
+            const int v = tid < kSortBins ? bins[tid] : 0;
+            const int off = block_exclusive_scan(v, tmp, &tot_l);
+            if (tid < kSortBins) bins[tid] = off;
+            long_base = tot_l;
+            __syncthreads();
+        }
+        if (static_cast<long long>(long_base) * hkv > p.max_long) {
+            if (tid == 0) s_overflow = 1;
+        } else {
+            for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+                const ReqInfo r = req(b);
+                for (int qt = 0; qt < r.qtiles; ++qt) {
+                    const int nvalid = min(p.q_tile_tokens, r.n - qt * p.q_tile_tokens);
+                    LongItem it{};
+                    it.b = b;
+                    it.q_tile = qt;
+                    it.key_begin = 0;
+                    it.key_end = min(r.len, r.ctx + qt * p.q_tile_tokens + nvalid);
+                    store_record(p.long_items, atomicAdd(&bins[long_bin(p, r, qt)], 1), it);
+                }
             }
         }
     }
@@ -352,7 +475,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
 
 int launch_plan(const PlanParams &p, cudaStream_t s) {
     PdlLaunch l(1, kPlanThreads, 0, s);
-    return cudaLaunchKernelEx(&l.cfg, plan_kernel, p) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return launch_kernel(l, plan_kernel, p) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace pa

@@ -420,15 +420,22 @@ __global__ void __launch_bounds__(kShortThreads, 2)
         // The next item's index, descriptor, length and first block ids are
         // fetched one step per stage while the current item is still being
         // issued, and block ids are read one 8-stage batch ahead, so the ring
-        // never waits on a chain of dependent global loads.
-        int cur_idx = 0;
-        if (lane == 0) cur_idx = atomicAdd(&p.hdr->short_next, 1);
-        cur_idx = __shfl_sync(0xffffffffu, cur_idx, 0);
+        // never waits on a chain of dependent global loads.  When the grid
+        // starts at once (it waited for the plan), CTA c starts with item c;
+        // beside a tensor-core grid, CTAs start as SMs free up and every item
+        // comes from the counter, so the longest items go to the CTAs that
+        // start first.
+        const int first_static = p.no_start_wait ? 0 : static_cast<int>(gridDim.x);
+        int cur_idx = blockIdx.x;
+        if (p.no_start_wait) {
+            if (lane == 0) cur_idx = atomicAdd(&p.hdr->short_next, 1);
+            cur_idx = __shfl_sync(0xffffffffu, cur_idx, 0);
+        }
         ShortItem cur{};
         int cur_h = 0, cur_L = 0, cur_row = -1;
         if (cur_idx < num_items) {
             cur = short_work(p, cur_idx, cur_h);
-            cur_L = __ldg(p.seq_lens + cur.b);
+            cur_L = cur.seq_len;
             cur_row = chunk_row_of(p, cur, cur_h, cur_L, cur.stage_begin, lane);
         }
         while (!aborted) {
@@ -447,7 +454,8 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                 break;
             }
             int nxt_idx = 0;
-            if (lane == 0) nxt_idx = atomicAdd(&p.hdr->short_next, 1);  // read two stages later
+            if (lane == 0)  // read two stages later
+                nxt_idx = atomicAdd(&p.hdr->short_next, 1) + first_static;
             ShortItem nxt{};
             int nxt_h = 0, nxt_L = 0, nxt_row = -1, pf = 0;  // prefetch state of the next item
             const int nst = cur.stage_end - cur.stage_begin;  // planner stages
@@ -502,12 +510,11 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                         if (nxt_idx < num_items) nxt = short_work(p, nxt_idx, nxt_h);
                         pf = 1;
                     } else if (pf == 1 && (rel >= 3 || rel == nrs - 1)) {
-                        if (nxt_idx < num_items) nxt_L = __ldg(p.seq_lens + nxt.b);
-                        pf = 2;
-                    } else if (pf == 2 && (rel >= 4 || rel == nrs - 1)) {
-                        if (nxt_idx < num_items)
+                        if (nxt_idx < num_items) {
+                            nxt_L = nxt.seq_len;
                             nxt_row = chunk_row_of(p, nxt, nxt_h, nxt_L, nxt.stage_begin, lane);
-                        pf = 3;
+                        }
+                        pf = 2;
                     } else {
                         break;
                     }
@@ -559,7 +566,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
             cs.tok0 = __ldg(p.qsl + item.b) + item.q_begin;
             const int n = item.q_count;
             cs.ctx = __ldg(p.ctx + item.b) + item.q_begin;
-            const int L = __ldg(p.seq_lens + item.b);
+            const int L = item.seq_len;
             cs.key_end = min(item.stage_end * kStageKeys, L);
             cs.R = n * p.group;
             cs.partial_base = item.partial_base + item_h * item.nsplit * cs.R;
@@ -956,17 +963,12 @@ __global__ void __launch_bounds__(kShortThreads, 2)
             }
             if (cs.nsplit > 1) {
                 // fused split-KV epilogue: the last split of (b, h) folds all
-                // partials.  One thread releases this CTA's partial writes
-                // (ordered before it by the CTA barrier) with a GPU-scope fence
-                // and the counter update, and acquires the others' if last.
+                // partials.  One thread's acquire-release counter update
+                // releases this CTA's partial writes (ordered before it by the
+                // CTA barrier) and, if it is the last, acquires the others'.
                 named_bar_sync(1, 32 * kShortConsumerWarps);
-                if (threadIdx.x == 0) {
-                    __threadfence();
-                    const int old = atomicAdd(p.counters + cs.counter, 1);
-                    const int last = (old == cs.nsplit - 1) ? 1 : 0;
-                    if (last) __threadfence();
-                    ctl[1] = last;
-                }
+                if (threadIdx.x == 0)
+                    ctl[1] = atomic_add_acq_rel_gpu(p.counters + cs.counter, 1) == cs.nsplit - 1;
                 named_bar_sync(1, 32 * kShortConsumerWarps);
                 if (*reinterpret_cast<volatile int *>(&ctl[1])) {
                     const int base = cs.partial_base - cs.split * cs.R;
@@ -1075,7 +1077,7 @@ static int launch(const ShortParams &p, const CUtensorMap &tk, const CUtensorMap
                   cudaStream_t s) {
     if (configure_short<D, FP8>() != PA_OK) return PA_ERR_CUDA;
     PdlLaunch l(grid, kShortThreads, ShortGeom<D, FP8>::kSmemBytes, s);
-    return cudaLaunchKernelEx(&l.cfg, short_kernel<D, FP8>, p, tk, tv) == cudaSuccess
+    return launch_kernel(l, short_kernel<D, FP8>, p, tk, tv) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
 }

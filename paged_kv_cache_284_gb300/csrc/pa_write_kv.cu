@@ -97,8 +97,8 @@ int launch_write_kv(const void *k, const void *v, const int64_t *slots, int num_
         const int threads = 256;
         const int64_t blocks = (total + threads - 1) / threads;
         PdlLaunch l(static_cast<unsigned>(blocks), threads, 0, s);
-        const cudaError_t e = cudaLaunchKernelEx(
-            &l.cfg, write_kv_fp8_kernel, static_cast<const uint4 *>(k),
+        const cudaError_t e = launch_kernel(
+            l, write_kv_fp8_kernel, static_cast<const uint4 *>(k),
             static_cast<const uint4 *>(v), slots, num_tokens, kv->num_kv_heads, pieces,
             kv->block_size, kv->num_blocks, kv->k_scale, kv->v_scale,
             static_cast<uint4 *>(kv->k_cache), static_cast<uint4 *>(kv->v_cache), status);
@@ -109,8 +109,8 @@ int launch_write_kv(const void *k, const void *v, const int64_t *slots, int num_
     const int threads = 256;
     const int64_t blocks = (total + threads - 1) / threads;
     PdlLaunch l(static_cast<unsigned>(blocks), threads, 0, s);
-    const cudaError_t e = cudaLaunchKernelEx(
-        &l.cfg, write_kv_kernel, static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slots,
+    const cudaError_t e = launch_kernel(
+        l, write_kv_kernel, static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slots,
         num_tokens, kv->num_kv_heads, pieces, kv->block_size, kv->num_blocks,
         static_cast<uint4 *>(kv->k_cache), static_cast<uint4 *>(kv->v_cache), status);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -188,8 +188,8 @@ int launch_stage_fp8(const pa_kv_desc *kv, const int32_t *block_tables, int32_t 
     // 16 codes per piece; a block holds num_kv_heads * block_size * head_dim codes
     const int pieces = kv->num_kv_heads * kv->block_size * kv->head_dim / 16;
     PdlLaunch l(static_cast<unsigned>(grid), 256, 0, s);
-    const cudaError_t e = cudaLaunchKernelEx(
-        &l.cfg, stage_fp8_kernel, static_cast<const uint4 *>(kv->k_cache),
+    const cudaError_t e = launch_kernel(
+        l, stage_fp8_kernel, static_cast<const uint4 *>(kv->k_cache),
         static_cast<const uint4 *>(kv->v_cache), kv->num_blocks, pieces, block_tables, bt_stride,
         hdr, stage_base, stage_list, static_cast<uint4 *>(stage_k), static_cast<uint4 *>(stage_v),
         status);

@@ -16,7 +16,8 @@ import oracle
 import paged_kv_cache_284_gb300 as pk
 from paged_kv_cache_284_gb300 import workloads
 from gpu_helpers import (DEV, assert_attention_close, assert_status_clean, bits, gpu_attend,
-                         gpu_write, oracle_attend, oracle_write, run_and_check)
+                         gpu_write, long_requests, oracle_attend, oracle_write,
+                         run_and_check)
 
 pytestmark = pytest.mark.gpu
 
@@ -237,4 +238,60 @@ def test_same_result_on_a_side_stream():
         o2, l2 = gpu_attend(step, kc, vc)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert_status_clean()
+
+
+def test_side_by_side_kernels_match_the_serial_launch_order():
+    """The step's default launch order runs the split-KV and tensor-core
+    kernels side by side (two tensor-core grids sharing a work counter); with
+    per-kernel profiling events set, the same kernels run one after the other
+    with a fixed item order.  Every item is computed the same way either
+    way, so the outputs agree bit for bit."""
+    pool, (step,) = workloads.mixed_step(num_chunks=4, chunk_len=256, chunk_ctx=(0, 3000),
+                                         num_decode=64, decode_len=(64, 3000), num_spec=8,
+                                         spec_ctx=(64, 3000))
+    assert len(long_requests(step)) == 4 and step.num_seqs > 4
+    kc, vc = pool.k_cache.to(DEV), pool.v_cache.to(DEV)
+    gpu_write(step, kc, vc)
+    out_a, lse_a = gpu_attend(step, kc, vc)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(2)]
+    for a, b in evs:
+        a.record()
+        b.record()
+    torch.cuda.synchronize()
+    pk.set_profile_events(pk.PA_KERNEL_SPLIT_KV, *evs[0])
+    pk.set_profile_events(pk.PA_KERNEL_TENSOR_CORE, *evs[1])
+    try:
+        out_b, lse_b = gpu_attend(step, kc, vc)
+        torch.cuda.synchronize()
+    finally:
+        pk.set_profile_events(pk.PA_KERNEL_SPLIT_KV, None, None)
+        pk.set_profile_events(pk.PA_KERNEL_TENSOR_CORE, None, None)
+    assert np.array_equal(bits(out_a), bits(out_b))
+    assert torch.equal(lse_a, lse_b)
+    assert_status_clean()
+
+
+def test_launches_per_step():
+    """The library's launch count for one step: write_kv, plan, split-KV and,
+    when the step can hold a long request (T >= 64 / group + 1 tokens), the
+    two tensor-core grids that run beside the split-KV grid."""
+    pool, (step,) = workloads.mixed_step(num_chunks=2, chunk_len=128, chunk_ctx=(0, 1000),
+                                         num_decode=16, decode_len=(64, 1000), num_spec=2,
+                                         spec_ctx=(64, 1000))
+    kc, vc = pool.k_cache.to(DEV), pool.v_cache.to(DEV)
+    torch.cuda.synchronize()
+    n0 = pk.kernel_launches()
+    gpu_write(step, kc, vc)
+    gpu_attend(step, kc, vc)
+    torch.cuda.synchronize()
+    assert pk.kernel_launches() - n0 == 5
+    dpool, (dstep,) = workloads.decode_heavy(num_seqs=8, lo=64, hi=600)
+    dkc, dvc = dpool.k_cache.to(DEV), dpool.v_cache.to(DEV)
+    n0 = pk.kernel_launches()
+    gpu_write(dstep, dkc, dvc)
+    gpu_attend(dstep, dkc, dvc)
+    torch.cuda.synchronize()
+    assert pk.kernel_launches() - n0 == 3
     assert_status_clean()
