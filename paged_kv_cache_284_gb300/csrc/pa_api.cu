@@ -142,6 +142,10 @@ struct ProfScope {
 
 // True while per-kernel profiling events are set: the step then launches its
 // kernels one after the other so that each event pair times one kernel.
+// Fewest query tokens for which a step runs its split-KV and tensor-core
+// kernels side by side (below it they run one after the other).
+constexpr int kSideBySideMinTokens = 512;
+
 bool profiling_active() {
     std::lock_guard<std::mutex> lock(g_prof_mu);
     return g_prof[PA_KERNEL_SPLIT_KV][0] || g_prof[PA_KERNEL_TENSOR_CORE][0];
@@ -422,14 +426,16 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
     const CUtensorMap &lk = staged ? stg.tk : maps.k;
     const CUtensorMap &lv = staged ? stg.tv : maps.v;
 
-    if (max_long_reqs > 0 && !profiling_active()) {
+    if (max_long_reqs > 0 && T >= kSideBySideMinTokens && !profiling_active()) {
         // The HBM-bound split-KV kernel and the tensor-core kernel run side by
         // side: a first tensor-core grid takes part of the SMs (it waits
         // for the plan, then lets the next grid in), the split-KV grid fills
         // the others, and a second tensor-core grid takes SMs over as
         // split-KV CTAs finish.  Both tensor-core grids pull items, longest
         // first, from the step's counter; the second completes only after
-        // the first and after the split-KV grid.
+        // the first and after the split-KV grid.  A step of few tokens has
+        // little or no tensor-core work: there the two extra launches would
+        // only add latency, and the kernels run one after the other.
         LongParams l1 = lp;
         l1.dynamic = 1;
         l1.wait_start = 1;

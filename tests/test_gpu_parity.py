@@ -276,10 +276,12 @@ def test_side_by_side_kernels_match_the_serial_launch_order():
 def test_launches_per_step():
     """The library's launch count for one step: write_kv, plan, split-KV and,
     when the step can hold a long request (T >= 64 / group + 1 tokens), the
-    two tensor-core grids that run beside the split-KV grid."""
-    pool, (step,) = workloads.mixed_step(num_chunks=2, chunk_len=128, chunk_ctx=(0, 1000),
+    tensor-core kernel -- as two grids beside the split-KV grid for a step
+    of at least 512 tokens, as one grid after it for a smaller step."""
+    pool, (step,) = workloads.mixed_step(num_chunks=2, chunk_len=256, chunk_ctx=(0, 1000),
                                          num_decode=16, decode_len=(64, 1000), num_spec=2,
                                          spec_ctx=(64, 1000))
+    assert step.num_q_tokens >= 512
     kc, vc = pool.k_cache.to(DEV), pool.v_cache.to(DEV)
     torch.cuda.synchronize()
     n0 = pk.kernel_launches()
@@ -287,6 +289,13 @@ def test_launches_per_step():
     gpu_attend(step, kc, vc)
     torch.cuda.synchronize()
     assert pk.kernel_launches() - n0 == 5
+    spool, (sstep,) = workloads.tiny_prefill()   # 90 tokens: could hold a long request
+    skc, svc = spool.k_cache.to(DEV), spool.v_cache.to(DEV)
+    n0 = pk.kernel_launches()
+    gpu_write(sstep, skc, svc)
+    gpu_attend(sstep, skc, svc)
+    torch.cuda.synchronize()
+    assert pk.kernel_launches() - n0 == 4
     dpool, (dstep,) = workloads.decode_heavy(num_seqs=8, lo=64, hi=600)
     dkc, dvc = dpool.k_cache.to(DEV), dpool.v_cache.to(DEV)
     n0 = pk.kernel_launches()
