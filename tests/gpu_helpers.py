@@ -120,7 +120,8 @@ def plan_header(ws):
     """The step plan's header at the start of the workspace (white-box check):
     work items of the two kernels and the fp8 staging counts."""
     h = ws[:64].cpu().view(torch.int32).tolist()
-    return {"short_items": h[0], "long_items": h[1], "num_staged": h[6], "staged_blocks": h[7]}
+    return {"short_items": h[0], "long_items": h[1], "split_stages": h[4], "num_staged": h[6],
+            "staged_blocks": h[7]}
 
 
 def long_requests(step, short_max_rows=64):

@@ -16,7 +16,7 @@ import oracle
 import paged_kv_cache_284_gb300 as pk
 from paged_kv_cache_284_gb300 import workloads
 from gpu_helpers import (DEV, assert_attention_close, assert_status_clean, bits, gpu_attend,
-                         gpu_write, long_requests, oracle_attend, oracle_write,
+                         gpu_write, long_requests, oracle_attend, oracle_write, plan_header,
                          run_and_check)
 
 pytestmark = pytest.mark.gpu
@@ -303,4 +303,27 @@ def test_launches_per_step():
     gpu_attend(dstep, dkc, dvc)
     torch.cuda.synchronize()
     assert pk.kernel_launches() - n0 == 3
+    assert_status_clean()
+
+
+def test_small_decode_batch_is_cut_into_one_round_of_items():
+    """A decode batch too small to fill the persistent split-KV grid (8
+    requests x 8 kv heads) is cut so that each CTA gets about one item: the
+    split size is the smallest that keeps the item count within the grid
+    (one round), above the 4-stage floor; results stay at parity."""
+    pool, (step,) = workloads.decode_heavy(seed=58, num_seqs=8)
+    kc, vc = pool.k_cache.to(DEV), pool.v_cache.to(DEV)
+    ws = pk.alloc_workspace(pk.workspace_size(step.num_seqs, step.num_q_tokens,
+                                              step.num_q_heads, step.num_kv_heads,
+                                              step.head_dim), DEV)
+    gpu_write(step, kc, vc)
+    out, lse = gpu_attend(step, kc, vc, workspace=ws)
+    torch.cuda.synchronize()
+    h = plan_header(ws)
+    ctas = 2 * torch.cuda.get_device_properties(0).multi_processor_count  # 2 per SM here
+    assert 0.8 * ctas <= h["short_items"] <= ctas, h
+    assert h["split_stages"] > 4, h
+    kb, vb = oracle_write(step, bits(pool.k_cache), bits(pool.v_cache))
+    ref_o, ref_l = oracle_attend(step, kb, vb)
+    assert_attention_close(out, lse, ref_o, ref_l, "one-round split")
     assert_status_clean()
