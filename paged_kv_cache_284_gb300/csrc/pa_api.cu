@@ -410,7 +410,6 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
         lp.prefix_mode = 0;
         lp.hdr = hdr;
         lp.items = pp.long_items;
-        lp.counters = pp.counters;
         lp.partial_o = sp.partial_o;
         lp.partial_lse = sp.partial_lse;
         lp.status = dev->status;
@@ -526,10 +525,6 @@ int run_prefix(const void *q, const pa_kv_desc *kv, const int32_t *prefix_blocks
     const int group = Hq / kv->num_kv_heads;
     int q_tiles, nsplit, split_keys;
     prefix_plan(T, prefix_len, kv->num_kv_heads, group, dev->sms, &q_tiles, &nsplit, &split_keys);
-    int *counters = reinterpret_cast<int *>(ws + L.counters);
-    if (nsplit > 1 &&
-        cudaMemsetAsync(counters, 0, sizeof(int) * kv->num_kv_heads * q_tiles, s) != cudaSuccess)
-        return fail(PA_ERR_CUDA, "counter reset failed");
     LongParams lp{};
     lp.out = static_cast<__nv_bfloat16 *>(out);
     lp.lse = lse;
@@ -550,13 +545,31 @@ int run_prefix(const void *q, const pa_kv_desc *kv, const int32_t *prefix_blocks
     lp.prefix_nsplit = nsplit;
     lp.prefix_split_keys = split_keys;
     lp.prefix_q_tiles = q_tiles;
-    lp.counters = counters;
+    // a split prefix leaves its split states to the fold kernel, which runs
+    // the fold of a (kv head, query tile) on many SMs
     lp.partial_o = reinterpret_cast<float *>(ws + L.partial_o);
     lp.partial_lse = reinterpret_cast<float *>(ws + L.partial_lse);
     lp.status = dev->status;
     const int grid = kv->num_kv_heads * q_tiles * nsplit;
-    const int rc = launch_long(lp, maps.q, maps.k, maps.v, kv->head_dim, grid, s);
+    int rc = launch_long(lp, maps.q, maps.k, maps.v, kv->head_dim, grid, s);
     if (rc != PA_OK) return fail(rc, "prefix kernel launch failed");
+    if (nsplit > 1) {
+        PrefixFoldParams f{};
+        f.partial_o = lp.partial_o;
+        f.partial_lse = lp.partial_lse;
+        f.nsplit = nsplit;
+        f.q_tiles = q_tiles;
+        f.pairs = kv->num_kv_heads * q_tiles;
+        f.group = group;
+        f.q_tile_tokens = lp.q_tile_tokens;
+        f.num_q_tokens = T;
+        f.num_q_heads = Hq;
+        f.out = static_cast<__nv_bfloat16 *>(out);
+        f.out_f32 = out_f32;
+        f.lse = lse;
+        rc = launch_prefix_fold(f, kv->head_dim, s);
+        if (rc != PA_OK) return fail(rc, "prefix fold launch failed");
+    }
     return PA_OK;
 }
 

@@ -143,7 +143,6 @@ struct LongParams {
     int prefix_len, prefix_nsplit, prefix_split_keys, prefix_q_tiles;
     PlanHeader *hdr;
     const LongItem *items;
-    int *counters;
     float *partial_o, *partial_lse;
     unsigned *status;
     // fp8 pool with a bf16 staging copy: request b's key block j is staging
@@ -188,6 +187,17 @@ struct PlanParams {
     int *counters;
     int max_short, max_long, cap_rows, num_counters;
     unsigned *status;
+};
+
+// Merge of the prefix pass's split states: item (kv head h, query tile qt,
+// split s) wrote row r of its tile at partial row
+// ((h * q_tiles + qt) * nsplit + s) * 128 + r.
+struct PrefixFoldParams {
+    const float *partial_o, *partial_lse;
+    int nsplit, q_tiles, pairs, group, q_tile_tokens, num_q_tokens, num_q_heads;
+    __nv_bfloat16 *out;  // bf16 result, or
+    float *out_f32;      // fp32 result (a state for the suffix pass)
+    float *lse;          // may be NULL
 };
 
 // Launch configuration with the programmatic-stream-serialisation attribute
@@ -235,6 +245,7 @@ int launch_short(const ShortParams &p, const CUtensorMap &tk, const CUtensorMap 
 int short_max_ctas_per_sm(int head_dim, bool fp8);
 int launch_long(const LongParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                 const CUtensorMap &tv, int head_dim, int grid, cudaStream_t s);
+int launch_prefix_fold(const PrefixFoldParams &f, int head_dim, cudaStream_t s);
 int launch_merge(const void *oa, const float *la, const void *ob, const float *lb, int n,
                  int heads, int head_dim, void *out, float *lse_out, cudaStream_t s);
 size_t short_smem_bytes(int head_dim);

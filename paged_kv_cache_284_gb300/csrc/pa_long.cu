@@ -24,9 +24,10 @@
 //    update, rescale O in TMEM only when the max grows by more than 2^8, and
 //    write P (bf16) into one of two TMEM P buffers; P V trails Q K^T by two
 //    tiles so the tensor cores always have the next scores to compute;
-//  * the epilogue reads O from TMEM, normalises and stores bf16 (or fp32
-//    partial states that the last split folds with the merge operator)
-//    while the next item's Q, K and V are already streaming in.
+//  * the epilogue reads O from TMEM, normalises and stores bf16 (or, for a
+//    split prefix, fp32 split states that prefix_fold_kernel merges with the
+//    merge operator) while the next item's Q, K and V are already streaming
+//    in.
 // Key tiles entirely above a tile's causal limit are never visited.
 #include "pa_internal.cuh"
 
@@ -81,21 +82,11 @@ struct Bars {
     uint64_t p_full[2];  // by tile parity: a softmax half may run a tile ahead
     uint64_t pv_done[2];  // P V of a tile finished, by the tile's P buffer
     uint64_t xchg[4];  // row-half exchange, one per TMEM lane quarter (2 warps each)
-    uint64_t o_free, sync, drain, drain_pv;
+    uint64_t o_free, drain, drain_pv;
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
     return warp_mbar_wait(bar, parity, abort);
-}
-
-// Barrier among the softmax warps built on an mbarrier with a bounded
-// wait, so a kernel that gave up elsewhere can never hang here.
-__device__ __forceinline__ bool softmax_sync(uint64_t *bar, uint32_t &phase, volatile int *abort) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-    const bool ok = warp_wait(bar, phase & 1, abort);
-    ++phase;
-    return ok;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -135,7 +126,7 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // Everything one role needs to know about a work item.
 struct Item {
     int b, h, tok0, nvalid, pos0, key_begin, key_end, causal, nsplit, split;
-    int counter_idx, partial_base, nt;
+    int pair, partial_base, nt;
 };
 
 __device__ __forceinline__ Item decode_item(const LongParams &p, int idx) {
@@ -164,8 +155,8 @@ __device__ __forceinline__ Item decode_item(const LongParams &p, int idx) {
         it.nvalid = min(TQ, p.num_q_tokens - it.tok0);
         it.key_begin = it.split * p.prefix_split_keys;
         it.key_end = min(p.prefix_len, it.key_begin + p.prefix_split_keys);
-        it.counter_idx = it.h * p.prefix_q_tiles + qt;
-        it.partial_base = it.counter_idx * it.nsplit * kLongRows;
+        it.pair = it.h * p.prefix_q_tiles + qt;
+        it.partial_base = it.pair * it.nsplit * kLongRows;
     }
     const int span = it.key_end - it.key_begin;
     it.nt = span > 0 ? (span + kLongKeys - 1) / kLongKeys : 0;
@@ -381,12 +372,10 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
         mbar_init(&bars->pv_done[0], 1);
         mbar_init(&bars->pv_done[1], 1);
         mbar_init(&bars->o_free, kSoftmaxWarps);
-        mbar_init(&bars->sync, kSoftmaxWarps);
         for (int i = 0; i < 4; ++i) mbar_init(&bars->xchg[i], 2);
         mbar_init(&bars->drain, 1);
         mbar_init(&bars->drain_pv, 1);
         ctl[0] = 0;
-        ctl[1] = 0;
         *sched.pub = 0;
         for (int w = 0; w < kLongWarps; ++w) sched.cons[w] = 0;
         fence_mbar_init();
@@ -528,7 +517,7 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
         const int jh = r - ttok * p.group;
         const int c0 = half * (kLongKeys / 2);  // first S / P column of this half
         const int o0 = half * (D / 2);          // first O column of this half
-        uint32_t t = 0, sync_phase = 0, x_phase = 0;
+        uint32_t t = 0, x_phase = 0;
         bool ok = true;
         // swap one float with the other half of the row (same row, other warp)
         float *xch = reinterpret_cast<float *>(smem + G::kOffXchg);
@@ -744,60 +733,6 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                     __stcg(p.partial_lse + prow, lse_v);
                 }
             }
-            if (!direct) {
-                // fused split epilogue: the last split of this (kv head, query
-                // tile) folds the partial states with the merge operator; each
-                // half of a row folds its own D/2 columns
-                __threadfence();
-                bool sok = softmax_sync(&bars->sync, sync_phase, abort_flag);
-                if (sok && r == 0 && half == 0) {
-                    const int old = atomicAdd(p.counters + it.counter_idx, 1);
-                    ctl[1] = (old == it.nsplit - 1) ? 1 : 0;
-                }
-                sok = softmax_sync(&bars->sync, sync_phase, abort_flag) && sok;
-                const int last = *reinterpret_cast<volatile int *>(&ctl[1]);
-                sok = softmax_sync(&bars->sync, sync_phase, abort_flag) && sok;  // flag read by all
-                if (sok && last && row_valid) {
-                    __threadfence();
-                    const int64_t base = it.partial_base + r;
-                    float M = -INFINITY;
-                    for (int s2 = 0; s2 < it.nsplit; ++s2)
-                        M = fmaxf(M, __ldcg(p.partial_lse + base + s2 * kLongRows));
-                    float wsum = 0.f;
-                    float w[64];
-                    const int ns = min(it.nsplit, 64);
-                    for (int s2 = 0; s2 < ns; ++s2) {
-                        const float ls = __ldcg(p.partial_lse + base + s2 * kLongRows);
-                        w[s2] = M == -INFINITY ? 0.f : __expf(ls - M);
-                        wsum += w[s2];
-                    }
-                    const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
-                    for (int e4 = o0 / 4; e4 < (o0 + D / 2) / 4; ++e4) {
-                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                        for (int s2 = 0; s2 < ns; ++s2) {
-                            const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-                                                        p.partial_o + (base + s2 * kLongRows) * D) + e4);
-                            acc.x += w[s2] * v.x;
-                            acc.y += w[s2] * v.y;
-                            acc.z += w[s2] * v.z;
-                            acc.w += w[s2] * v.w;
-                        }
-                        acc.x *= winv;
-                        acc.y *= winv;
-                        acc.z *= winv;
-                        acc.w *= winv;
-                        if (p.out_f32) {
-                            reinterpret_cast<float4 *>(p.out_f32 + orow * D)[e4] = acc;
-                        } else {
-                            uint2 pk2;
-                            pk2.x = pack_bf16x2(acc.x, acc.y);
-                            pk2.y = pack_bf16x2(acc.z, acc.w);
-                            reinterpret_cast<uint2 *>(p.out + orow * D)[e4] = pk2;
-                        }
-                    }
-                    if (p.lse && half == 0) p.lse[orow] = wsum > 0.f ? M + __logf(wsum) : -INFINITY;
-                }
-            }
             t += it.nt;
         }
     }
@@ -827,6 +762,85 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
             __threadfence();
         }
     }
+}
+
+// Merge of the prefix pass's split states with the merge operator (2048ai.net
+// page on the vLLM V1 engine, §02.1 级联推理): one warp per query row of a
+// (kv head, query tile), its lanes across the head dimension, so that all
+// splits' loads of a row are in flight at once and the work spreads over
+// many SMs (one CTA per 8 rows).  A split count of at most 64 is assumed.
+template <int D>
+__global__ void __launch_bounds__(256) prefix_fold_kernel(const PrefixFoldParams f) {
+    pdl_wait();  // the prefix pass's states
+    const int lane = threadIdx.x & 31;
+    const int64_t w = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int pair = static_cast<int>(w / kLongRows), r = static_cast<int>(w % kLongRows);
+    if (pair >= f.pairs || r >= f.q_tile_tokens * f.group) return;
+    const int ttok = r / f.group, jh = r - ttok * f.group;
+    const int h = pair / f.q_tiles, qt = pair - h * f.q_tiles;
+    const int tok = qt * f.q_tile_tokens + ttok;
+    if (tok >= f.num_q_tokens) return;
+    const int ns = f.nsplit;
+    const int64_t base = static_cast<int64_t>(pair) * ns * kLongRows + r;
+    // split s's log-sum-exp lives in lane s % 32, slot s / 32
+    const float l0 = lane < ns ? __ldcg(f.partial_lse + base + lane * kLongRows) : -INFINITY;
+    const float l1 = lane + 32 < ns ? __ldcg(f.partial_lse + base + (lane + 32) * kLongRows)
+                                    : -INFINITY;
+    float M = fmaxf(l0, l1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w0 = (lane < ns && M != -INFINITY) ? __expf(l0 - M) : 0.f;
+    const float w1 = (lane + 32 < ns && M != -INFINITY) ? __expf(l1 - M) : 0.f;
+    float wsum = w0 + w1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    const bool col = lane < D / 4;  // this lane's float4 of the row
+    const float4 *po = reinterpret_cast<const float4 *>(f.partial_o + base * D) + (col ? lane : 0);
+    const int64_t stride = static_cast<int64_t>(kLongRows) * (D / 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < ns; s0 += 8) {
+        float ws[8];
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int s = s0 + j;
+            const float a = __shfl_sync(0xffffffffu, w0, s & 31);
+            const float b = __shfl_sync(0xffffffffu, w1, s & 31);
+            ws[j] = s < ns ? (s < 32 ? a : b) : 0.f;
+            v[j] = (col && s < ns) ? __ldcg(po + s * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            acc.x += ws[j] * v[j].x;
+            acc.y += ws[j] * v[j].y;
+            acc.z += ws[j] * v[j].z;
+            acc.w += ws[j] * v[j].w;
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const int64_t row = static_cast<int64_t>(tok) * f.num_q_heads + h * f.group + jh;
+    if (col) {
+        const float4 a = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (f.out_f32) {
+            reinterpret_cast<float4 *>(f.out_f32 + row * D)[lane] = a;
+        } else {
+            uint2 pk2;
+            pk2.x = pack_bf16x2(a.x, a.y);
+            pk2.y = pack_bf16x2(a.z, a.w);
+            reinterpret_cast<uint2 *>(f.out + row * D)[lane] = pk2;
+        }
+    }
+    if (lane == 0 && f.lse) f.lse[row] = wsum > 0.f ? M + __logf(wsum) : -INFINITY;
+}
+
+int launch_prefix_fold(const PrefixFoldParams &f, int head_dim, cudaStream_t s) {
+    const int64_t warps = static_cast<int64_t>(f.pairs) * kLongRows;
+    const unsigned grid = static_cast<unsigned>((warps + 7) / 8);
+    if (grid == 0) return PA_OK;
+    PdlLaunch l(grid, 256, 0, s);
+    const cudaError_t e = head_dim == 128 ? launch_kernel(l, prefix_fold_kernel<128>, f)
+                                          : launch_kernel(l, prefix_fold_kernel<64>, f);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 size_t long_smem_bytes(int head_dim) {
