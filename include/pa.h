@@ -234,8 +234,9 @@ size_t pa_cascade_workspace_size(int32_t num_seqs, int32_t num_q_tokens, int32_t
  * §02.1): every query row attends all prefix_len keys held, in order, by the
  * physical blocks prefix_blocks[0 .. ceil(prefix_len/bs)) (int32, device),
  * with no mask.  Each prefix block is loaded once per (kv head, 128 query
- * rows), not once per request.  Writes bf16 out and fp32 lse (may be NULL)
- * shaped as in pa_attention.
+ * rows), not once per request; the key range is split over the SMs and the
+ * splits' states are merged by a second launch within the call.  Writes
+ * bf16 out and fp32 lse (may be NULL) shaped as in pa_attention.
  */
 int pa_prefix_attention(const void *q, const pa_kv_desc *kv, const int32_t *prefix_blocks,
                         int32_t prefix_len, int32_t num_q_tokens, int32_t num_q_heads,
