@@ -327,3 +327,24 @@ def test_small_decode_batch_is_cut_into_one_round_of_items():
     ref_o, ref_l = oracle_attend(step, kb, vb)
     assert_attention_close(out, lse, ref_o, ref_l, "one-round split")
     assert_status_clean()
+
+
+def test_cascade_with_64_prefix_splits():
+    """One query tile per kv head (8 requests x 4 heads of 2 kv heads) over an
+    8192-token prefix: the prefix pass cuts it into 64 key-range splits, the
+    most it makes, so the fold merges states 32-63 too."""
+    pool, (step,) = workloads.cascade(seed=64, num_seqs=8, prefix_len=8192, suffix=(1, 200),
+                                      num_q_heads=8, num_kv_heads=2)
+    kc, vc = pool.k_cache.to(DEV), pool.v_cache.to(DEV)
+    gpu_write(step, kc, vc)
+    kb, vb = oracle_write(step, bits(pool.k_cache), bits(pool.v_cache))
+    q = step.q.to(DEV)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=DEV)
+    pk.pa_cascade_decode(q, kc, vc, step.prefix_blocks.to(DEV), step.prefix_len,
+                         step.suffix_block_tables.to(DEV), step.query_start_loc.to(DEV),
+                         step.suffix_context_lens.to(DEV), step.suffix_seq_lens.to(DEV),
+                         step.scale, out, lse)
+    ro, rl = oracle_attend(step, kb, vb)
+    assert_attention_close(out, lse, ro, rl, "cascade, 64 prefix splits")
+    assert_status_clean()
