@@ -204,17 +204,25 @@ int pa_merge_states(const void *o_a, const float *lse_a, const void *o_b, const 
  * counterpart on the pages: this is a deployment convenience).  Same
  * arguments and results as pa_attention, without the workspace: the
  * library keeps its scratch (work list, split partial states, counters) in
- * one fixed device array of PA_NO_ALLOC_SCRATCH_BYTES that every GPU which
- * loads the library holds until the process exits.  The call allocates
+ * one fixed device array of PA_NO_ALLOC_SCRATCH_BYTES.  The call allocates
  * nothing and frees nothing.
- *  - The first call on each device looks up the array's device address
- *    (with that device current); make it before any stream capture.
+ *  - The array is committed on a device when this entry point is first
+ *    called there (its module is loaded lazily; that first call also looks
+ *    up the array's device address, with the device current) and is held
+ *    until the process exits.  Make one call at start-up on each device you
+ *    will use -- it may fail with PA_ERR_CUDA if the device is out of
+ *    memory -- and before any stream capture.
  *  - All calls on a device share the array and it keeps the last call's
  *    contents: calls whose kernels overlap on the GPU race and give wrong
  *    results.  Order them (one stream, or events).
- *  - A step whose work list does not fit returns PA_ERR_WORKSPACE with a
- *    message; when little room is left for split-KV partial states the
- *    planner simply uses longer splits.
+ *  - A step whose work lists do not fit returns PA_ERR_WORKSPACE with a
+ *    message.  The work lists get the least room that always fits, and the
+ *    split-KV partial states what is left, so large batches may be cut into
+ *    fewer, longer splits than pa_attention would choose (same results up
+ *    to rounding).
+ *  - On an fp8 (e4m3) pool there is no staging room for the tensor-core
+ *    path: every request runs on the split-KV kernel (long ones in pieces of
+ *    64 / group query tokens).
  */
 #define PA_NO_ALLOC_SCRATCH_BYTES (32u << 20)
 int pa_attention_no_alloc(const void *q, const pa_kv_desc *kv, const int32_t *block_tables,

@@ -7,20 +7,30 @@
 // runs where allocation is forbidden or unsafe (a memory-pressure or shutdown
 // path of a serving engine, or a plugin that must not create device buffers
 // of its own).  This entry point serves them: its scratch is one fixed array
-// in the library's own device memory, created when the library is loaded on a
-// device, so a call only needs the inputs and outputs.
+// in the library's own device memory, so a call only needs the inputs and
+// outputs.
 //
 // Costs and rules for users:
-//  * every GPU that loads the library holds PA_NO_ALLOC_SCRATCH_BYTES of device
-//    memory for this array until the process exits;
+//  * this file is its own device module, and under lazy module loading (the
+//    CUDA default) a module is loaded on a device when the library first
+//    needs it there: the array's PA_NO_ALLOC_SCRATCH_BYTES are committed on a
+//    device at the first call of this entry point on that device (which looks
+//    up the array's address), and held until the process exits.  A caller
+//    that must not allocate later should make one call at start-up on every
+//    device it will use -- that first call can fail with PA_ERR_CUDA if the
+//    device has no room left -- and before any stream capture begins;
 //  * all calls on a device share the one array and it keeps the last call's
 //    contents: calls whose kernels overlap on the GPU (other streams, other
 //    host threads) race on it and give wrong results -- order them;
-//  * the first call on each device looks up the array's device address; make
-//    that first call before any stream capture begins;
-//  * a step whose work list does not fit the array is refused with
-//    PA_ERR_WORKSPACE and a message; smaller split-KV partial space only makes
-//    the planner choose longer splits.
+//  * a step whose work lists do not fit the array is refused with
+//    PA_ERR_WORKSPACE and a message.  The work lists get the smallest room
+//    that always fits one split per request piece and kv head, and the
+//    partial-state area whatever is left, so a large batch may be given
+//    longer (fewer) splits than pa_attention would choose -- same results,
+//    up to rounding;
+//  * on an fp8 (e4m3) pool there is no room for the bf16 staging copy the
+//    tensor-core path reads, so every request (long ones in pieces of
+//    64 / group query tokens) runs on the split-KV kernel.
 #include <mutex>
 
 #include "pa_internal.cuh"
