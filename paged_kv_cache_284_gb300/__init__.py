@@ -40,7 +40,9 @@ EXPORTED = ["pa_write_kv", "pa_attention_workspace_size", "pa_attention", "pa_at
             "pa_bm_create", "pa_bm_destroy", "pa_bm_add_request", "pa_bm_append_tokens",
             "pa_bm_fork", "pa_bm_schedule", "pa_bm_free_request", "pa_bm_num_free_blocks",
             "pa_bm_num_cached_blocks", "pa_bm_block_ref_count", "pa_bm_request_blocks",
-            "pa_bm_num_computed"]
+            "pa_bm_num_computed",
+            # request router for sharded replicas (include/pa_shard.h)
+            "pa_partition_requests"]
 PA_KERNEL_WRITE_KV, PA_KERNEL_PLAN, PA_KERNEL_SPLIT_KV, PA_KERNEL_TENSOR_CORE = range(4)
 
 
@@ -103,6 +105,7 @@ def _declare(lib):
         "pa_bm_block_ref_count": ([P, i32], i32),
         "pa_bm_request_blocks": ([P, i64, P, i32], i32),
         "pa_bm_num_computed": ([P, i64], i32),
+        "pa_partition_requests": ([P, i32, i32, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -311,6 +314,21 @@ def pa_validate_metadata(block_tables, query_start_loc, context_lens, seq_lens, 
     _check(lib().pa_validate_metadata(_ptr(bt), int(bt.shape[1]), _ptr(qsl), _ptr(ctx), _ptr(sl),
                                       int(sl.shape[0]), T, _ptr(sm), int(num_blocks),
                                       int(block_size)), "pa_validate_metadata")
+
+
+def partition_requests(seq_lens, num_ranks: int):
+    """Request router for request-sharded replicas (host only): the rank of
+    each request, balancing KV tokens greedily longest first, and the KV
+    tokens each rank receives.  seq_lens: sequence of ints or a tensor."""
+    sl = torch.as_tensor(seq_lens, dtype=torch.int32).detach().cpu().contiguous()
+    n = int(sl.numel())
+    rank_of = torch.empty(n, dtype=torch.int32)
+    loads = torch.empty(max(int(num_ranks), 1), dtype=torch.int64)
+    rc = lib().pa_partition_requests(_ptr(sl) if n else None, n, int(num_ranks),
+                                     _ptr(rank_of) if n else None, _ptr(loads))
+    if rc != PA_OK:
+        raise PaError(rc, "pa_partition_requests", "bad sizes or a negative length")
+    return rank_of.tolist(), loads[:int(num_ranks)].tolist()
 
 
 def read_device_status(clear: bool = True, stream=None) -> int:

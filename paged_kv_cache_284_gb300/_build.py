@@ -17,7 +17,7 @@ OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpa.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 SOURCES = ["pa_api.cu", "pa_write_kv.cu", "pa_plan.cu", "pa_short.cu", "pa_long.cu",
-           "pa_merge.cu", "pa_static.cu", "pa_blocks.cpp"]
+           "pa_merge.cu", "pa_static.cu", "pa_blocks.cpp", "pa_shard.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

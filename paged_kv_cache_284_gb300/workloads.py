@@ -269,6 +269,42 @@ def decode_heavy(seed: int = SEED_BASE + 2, num_seqs: int = 256, lo: int = 512,
     return pool, [step]
 
 
+def _mixed_requests(gen, num_chunks, chunk_len, chunk_ctx, num_decode, decode_len, num_spec,
+                    spec_len, spec_ctx):
+    dec = _uniform_int(decode_len[0], decode_len[1], num_decode, gen)
+    spec = _uniform_int(spec_ctx[0], spec_ctx[1], num_spec, gen)
+    chunks = _uniform_int(chunk_ctx[0], chunk_ctx[1], num_chunks, gen)
+    return ([(L - 1, 1) for L in dec] + [(c, spec_len) for c in spec]
+            + [(c, chunk_len) for c in chunks])
+
+
+def mixed_step_requests(seed: int = SEED_BASE + 3, num_chunks: int = 8, chunk_len: int = 512,
+                        chunk_ctx: Tuple[int, int] = (0, 8192), num_decode: int = 192,
+                        decode_len: Tuple[int, int] = (256, 8192), num_spec: int = 32,
+                        spec_len: int = 5, spec_ctx: Tuple[int, int] = (256, 8192)):
+    """The (context_len, q_len) list of mixed_step(seed) without building its
+    pool: the same draws, in the same order."""
+    gen = torch.Generator().manual_seed(seed)
+    return _mixed_requests(gen, num_chunks, chunk_len, chunk_ctx, num_decode, decode_len,
+                           num_spec, spec_len, spec_ctx)
+
+
+def from_requests(requests: Sequence[Tuple[int, int]], seed: int, num_q_heads: int = 32,
+                  num_kv_heads: int = 8, head_dim: int = 128, block_size: int = 16,
+                  label: str = "requests"):
+    """A pool and one step for a given [(context_len, q_len)] list, e.g. the
+    requests a router sent to one replica: blocks from a seeded permutation
+    of a pool sized to the blocks needed + 10 %, then q/k/v."""
+    gen = torch.Generator().manual_seed(seed)
+    reqs = list(requests)
+    nb, tables, _ = _assign_tables(reqs, block_size, gen)
+    pool = make_pool(nb, num_kv_heads, block_size, head_dim, gen)
+    step = build_step(reqs, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+                      head_dim=head_dim, block_size=block_size, gen=gen, tables=tables,
+                      label=label)
+    return pool, [step]
+
+
 def mixed_step(seed: int = SEED_BASE + 3, num_chunks: int = 8, chunk_len: int = 512,
                chunk_ctx: Tuple[int, int] = (0, 8192), num_decode: int = 192,
                decode_len: Tuple[int, int] = (256, 8192), num_spec: int = 32,
@@ -278,11 +314,8 @@ def mixed_step(seed: int = SEED_BASE + 3, num_chunks: int = 8, chunk_len: int = 
     """One mixed continuous-batching step: decode rows first, then
     speculative-verify rows (1 + 4 drafts), then chunked-prefill chunks."""
     gen = torch.Generator().manual_seed(seed)
-    dec = _uniform_int(decode_len[0], decode_len[1], num_decode, gen)
-    spec = _uniform_int(spec_ctx[0], spec_ctx[1], num_spec, gen)
-    chunks = _uniform_int(chunk_ctx[0], chunk_ctx[1], num_chunks, gen)
-    reqs = ([(L - 1, 1) for L in dec] + [(c, spec_len) for c in spec]
-            + [(c, chunk_len) for c in chunks])
+    reqs = _mixed_requests(gen, num_chunks, chunk_len, chunk_ctx, num_decode, decode_len,
+                           num_spec, spec_len, spec_ctx)
     nb, tables, _ = _assign_tables(reqs, block_size, gen)
     pool = make_pool(nb, num_kv_heads, block_size, head_dim, gen)
     step = build_step(reqs, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
