@@ -77,10 +77,10 @@ def test_fp8_write_quantises_out_of_range_values_by_saturation():
     assert_status_clean()
 
 
-def test_fp8_decode_heavy_full_size_sampled():
+def test_fp8_decode_heavy_full_size():
     """The decode-heavy step at full size on an e4m3 pool: every row finite and
-    inside the range of the values it averages; sampled requests against the
-    oracle one by one."""
+    inside the range of the values it averages, and every row against the
+    oracle over the dequantised codes."""
     pool, (step,) = workloads.decode_heavy()
     pool8 = workloads.fp8_pool_like(pool, 7012)
     del pool
@@ -95,14 +95,10 @@ def test_fp8_decode_heavy_full_size_sampled():
     assert o.abs().max().item() <= vmax * (1 + 2 ** -7)
     kb, vb = oracle.write_kv_fp8(step.k, step.v, step.slot_mapping, pool8.k_cache,
                                  pool8.v_cache, pool8.k_scale, pool8.v_scale)
-    idx = [0, 1, 77, 128, 200, step.num_seqs - 1]
-    sub = workloads.subset(step, idx)
-    ref_o, ref_l = oracle.attention_fp8(sub.q, kb, vb, pool8.k_scale, pool8.v_scale,
-                                        sub.block_tables, sub.query_start_loc,
-                                        sub.context_lens, sub.seq_lens, sub.scale)
-    qsl = step.query_start_loc
-    rows = torch.cat([torch.arange(int(qsl[b]), int(qsl[b + 1])) for b in idx]).to(DEV)
-    assert_attention_close(out[rows], lse[rows], ref_o, ref_l, "fp8 decode_heavy")
+    ref_o, ref_l = oracle.attention_fp8(step.q, kb, vb, pool8.k_scale, pool8.v_scale,
+                                        step.block_tables, step.query_start_loc,
+                                        step.context_lens, step.seq_lens, step.scale)
+    assert_attention_close(out, lse, ref_o, ref_l, "fp8 decode_heavy")
     assert_status_clean()
 
 
