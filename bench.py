@@ -262,6 +262,62 @@ def time_steps(fn, steps, stream):
     return start.elapsed_time(end)
 
 
+def sharded_mixed_step(world: int, rank: int):
+    """The job at N > 1 GPUs: N copies of the mixed-step recipe's requests
+    (seeds 284003 + 1000 i), routed to the N replicas by the library's
+    request router (KV tokens balanced, greedy longest first).  This rank
+    builds a pool and a step for its own requests only; no data crosses
+    ranks.  Returns (pool, step, global request list)."""
+    import paged_kv_cache_284_gb300 as pk
+    from paged_kv_cache_284_gb300 import workloads
+    reqs = []
+    for i in range(world):
+        reqs += workloads.mixed_step_requests(seed=workloads.SEED_BASE + 3 + 1000 * i)
+    rank_of, _ = pk.partition_requests([c + n for c, n in reqs], world)
+    mine = [reqs[b] for b in range(len(reqs)) if rank_of[b] == rank]
+    pool, (step,) = workloads.from_requests(mine, seed=workloads.SEED_BASE + 3 + 1000 * rank,
+                                            label=f"mixed step shard {rank}/{world}")
+    return pool, step, reqs
+
+
+def headline_config(args, world, step, pool, global_reqs=None):
+    """The `config` object of the JSON line, the same on both arms: the
+    whole job's requests, query tokens and KV bytes."""
+    fp8 = args.kv_dtype == "fp8"
+    elem = 1 if fp8 else 2
+    hkv, d = step.num_kv_heads, step.head_dim
+    if global_reqs is None:
+        reqs = [(int(c), int(n)) for c, n in zip(step.context_lens.tolist(),
+                                                 step.q_lens.tolist())]
+    else:
+        reqs = global_reqs
+    cfg = {"workload": (WORKLOAD if args.workload == "mixed_step" else step.label)
+           + ("; e4m3 KV pool, per-kv-head scales" if fp8 else ""),
+           "kv_dtype": args.kv_dtype,
+           "requests": len(reqs),
+           "query_tokens": sum(n for _, n in reqs),
+           "kv_bytes_read_per_step": sum(2 * (c + n) * hkv * d * elem for c, n in reqs),
+           "l2": "inputs larger than L2 (no flush needed)",
+           "parallelism": (f"{world} request-sharded replicas: the library's router splits "
+                           f"{world} copies of the step's requests over the GPUs by KV tokens; "
+                           f"no collective on the data path") if world > 1 else "single GPU",
+           "seed": 284003}
+    if world == 1:
+        cfg["pool_blocks"] = pool.num_blocks
+    return cfg
+
+
+def all_ranks_sum(x: int, device) -> int:
+    """Sum of an integer over ranks (each replica's query tokens); a no-op
+    without torch.distributed."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.int64, device=device)
+    dist.all_reduce(t)
+    return int(t.item())
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle baseline
 # ---------------------------------------------------------------------------
@@ -316,7 +372,11 @@ def run_reference(args):
     import oracle
     from paged_kv_cache_284_gb300 import workloads
     oracle.build_oracle()
-    pool, (step,) = workloads.mixed_step()
+    global_reqs = None
+    if world > 1:
+        pool, step, global_reqs = sharded_mixed_step(world, 0)
+    else:
+        pool, (step,) = workloads.mixed_step()
     sub = oracle_sample(pool, step)
     for _ in range(args.warmup):
         time_oracle(pool, sub)
@@ -326,14 +386,15 @@ def run_reference(args):
     tok = sub.num_q_tokens * args.steps
     value = tok / t
     cores = os.cpu_count()
-    sample = (f"1/8 of the mixed step per timed step ({sub.num_seqs} requests, "
-              f"{sub.num_q_tokens} query tokens): oracle write_kv + attention, fp64")
+    sample = (f"1/8 of the mixed step{' shard of rank 0' if world > 1 else ''} per timed "
+              f"step ({sub.num_seqs} requests, {sub.num_q_tokens} query tokens): oracle "
+              f"write_kv + attention, fp64")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "query tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * t / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "sample": sample},
+        "config": headline_config(args, world, step, pool, global_reqs),
         "cpu_baseline": {"value": value, "unit": "query tokens/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "query tokens/s", "h2d_bytes_per_step": 0,
@@ -360,8 +421,11 @@ def run_ours(args):
 
     # ---- headline: the mixed step ------------------------------------------
     t0 = time.time()
-    if args.workload == "mixed_step":
-        pool, (step,) = workloads.mixed_step(seed=workloads.SEED_BASE + 3 + 1000 * rank)
+    global_reqs = None
+    if args.workload == "mixed_step" and world > 1:
+        pool, step, global_reqs = sharded_mixed_step(world, rank)
+    elif args.workload == "mixed_step":
+        pool, (step,) = workloads.mixed_step()
     elif args.workload == "decode_heavy":
         pool, (step,) = workloads.decode_heavy(seed=workloads.SEED_BASE + 2 + 1000 * rank)
     else:  # the 8 prefill chunks of the mixed step alone
@@ -404,6 +468,7 @@ def run_ours(args):
     # the library's own count of the kernels it enqueued in the timed region
     gpu_launches = pk.kernel_launches() - launches0
     ms = max_over_ranks(ms, dev)
+    job_tokens = all_ranks_sum(step.num_q_tokens, dev)
     clocks = sampler.stop() if sampler else None
 
     # kernel pass: the same K steps with CUDA events around each launch of
@@ -428,7 +493,7 @@ def run_ours(args):
         log(f"[bench] WARNING device status {status:#x}")
 
     ms_step = ms / args.steps
-    value = job_throughput(world, step.num_q_tokens, args.steps, ms)
+    value = job_tokens * args.steps / (ms / 1000.0)
     short_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[pk.PA_KERNEL_SPLIT_KV])
     long_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[pk.PA_KERNEL_TENSOR_CORE])
     achieved = short_bytes / (short_ms / 1000.0) / 1e9 if short_bytes else 0.0
@@ -514,7 +579,7 @@ def run_ours(args):
         end.record(stream)
         end.synchronize()
         e_ms = max_over_ranks(start.elapsed_time(end), dev)
-        e2e = {"value": job_throughput(world, step.num_q_tokens, args.steps, e_ms),
+        e2e = {"value": job_tokens * args.steps / (e_ms / 1000.0),
                "unit": "query tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / args.steps,
                "copies": "pinned host buffers; uploads and downloads on a second stream, "
@@ -550,16 +615,7 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3 KV, f16 MMA" if fp8 else "bf16",
             "data": "synthetic",
-            "config": {"workload": (WORKLOAD if args.workload == "mixed_step" else step.label)
-                       + ("; e4m3 KV pool, per-kv-head scales" if fp8 else ""),
-                       "kv_dtype": args.kv_dtype,
-                       "requests": step.num_seqs,
-                       "query_tokens": step.num_q_tokens, "pool_blocks": pool.num_blocks,
-                       "kv_bytes_read_per_step": kv_bytes(step, range(step.num_seqs),
-                                                          1 if fp8 else 2),
-                       "l2": "inputs larger than L2 (no flush needed)",
-                       "parallelism": "replicas" if world > 1 else "single GPU",
-                       "seed": workloads.SEED_BASE + 3},
+            "config": headline_config(args, world, step, pool, global_reqs),
             "roofline": roofline,
             "kernels": {"split_kv": split_kv, "tensor_core": tensor_core},
             "decode_heavy": decode,
@@ -711,7 +767,7 @@ def bench_fp8(args, dev, hbm_peak):
     return res
 
 
-def bench_cascade(args, dev):
+def bench_cascade(args, dev, compare_full=True, parts=False):
     import paged_kv_cache_284_gb300 as pk
     from paged_kv_cache_284_gb300 import workloads
     pool, (step,) = workloads.cascade()
@@ -733,20 +789,53 @@ def bench_cascade(args, dev):
 
     for _ in range(max(3, args.warmup)):
         casc()
-        ds.run(write=False)
     torch.cuda.synchronize()
     ms_c = time_steps(casc, args.steps, torch.cuda.current_stream()) / args.steps
-    ms_p = time_steps(lambda: ds.run(write=False), args.steps,
-                      torch.cuda.current_stream()) / args.steps
+    ms_p = None
+    if compare_full:
+        for _ in range(max(3, args.warmup)):
+            ds.run(write=False)
+        torch.cuda.synchronize()
+        ms_p = time_steps(lambda: ds.run(write=False), args.steps,
+                          torch.cuda.current_stream()) / args.steps
+    if parts:
+        # the two passes on their own: the shared-prefix pass (bf16 output)
+        # and paged attention over the suffix tables alone
+        def prefix_only():
+            pk.pa_prefix_attention(ds.q, ds.kc, ds.vc, pb, step.prefix_len, step.scale, out,
+                                   lse, workspace=ws)
+
+        def suffix_only():
+            pk.pa_attention(ds.q, ds.kc, ds.vc, sbt, ds.qsl, sctx, ssl, step.scale, out, lse,
+                            workspace=ws)
+
+        part_ms = {}
+        for name, fn in (("prefix_pass_ms", prefix_only), ("suffix_pass_ms", suffix_only)):
+            for _ in range(max(3, args.warmup)):
+                fn()
+            torch.cuda.synchronize()
+            part_ms[name] = time_steps(fn, args.steps, torch.cuda.current_stream()) / args.steps
     uniq = sum(int(s) for s in step.suffix_seq_lens) * step.num_kv_heads * step.head_dim * 4
     pref = step.prefix_len * step.num_kv_heads * step.head_dim * 4
     res = {"workload": "64 requests sharing an 8192-token prefix, suffix U[128,1024], q_len 1",
-           "cascade_ms": ms_c, "paged_attention_ms": ms_p, "speedup": ms_p / ms_c,
+           "cascade_ms": ms_c, "paged_attention_ms": ms_p,
+           "speedup": ms_p / ms_c if ms_p else None,
            "cascade_algorithmic_kv_bytes": uniq + pref,
            "cascade_kv_gbs": (uniq + pref) / (ms_c / 1000) / 1e9}
+    if parts:
+        res.update(part_ms)
     del ds
     torch.cuda.empty_cache()
     return res
+
+
+def run_cascade_only(args):
+    """Profiling case: the cascade decode call alone (no write, no full-table
+    comparison), W warm-up calls then K timed calls; one JSON line."""
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    res = bench_cascade(args, dev, compare_full=False, parts=True)
+    print(json.dumps({"workload": "cascade", **res}), flush=True)
 
 
 def main():
@@ -760,7 +849,7 @@ def main():
                     help="KV pool element type of the headline step (fp8 = e4m3 + scales)")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--workload", choices=["mixed_step", "decode_heavy", "prefill"],
+    ap.add_argument("--workload", choices=["mixed_step", "decode_heavy", "prefill", "cascade"],
                     default="mixed_step",
                     help="headline workload (mixed_step is the benchmark; the others are "
                          "single-kernel cases for profiling)")
@@ -771,6 +860,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "cascade":
+        run_cascade_only(args)
     else:
         run_ours(args)
 

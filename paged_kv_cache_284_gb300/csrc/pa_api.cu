@@ -163,8 +163,10 @@ int pieces_bound(int num_seqs, int num_q_tokens, int group) {
     return num_seqs + (num_q_tokens + pt - 1) / pt;
 }
 
+// prefix_rows > 0: room for the cascade prefix pass's split states;
+// with_extra: room for cascade decode's fp32 suffix state ([T*Hq] rows).
 WsLayout make_layout(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads,
-                     int head_dim, int prefix_partial_rows, bool with_extra) {
+                     int head_dim, int prefix_rows, bool with_extra) {
     WsLayout L{};
     const int group = num_q_heads / num_kv_heads;
     const int tq = q_tile_tokens(group);
@@ -172,10 +174,7 @@ WsLayout make_layout(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv
     L.max_short = num_kv_heads * (num_seqs * 8 + pieces) + 4096;
     L.max_long = num_kv_heads * ((num_q_tokens + tq - 1) / tq + num_seqs);
     L.cap_rows = L.max_short * 4;
-    if (prefix_partial_rows > L.cap_rows) L.cap_rows = prefix_partial_rows;
     L.num_counters = num_kv_heads * std::max(1, pieces);
-    const int prefix_counters = num_kv_heads * ((num_q_tokens + tq - 1) / tq + 1);
-    if (with_extra && prefix_counters > L.num_counters) L.num_counters = prefix_counters;
     size_t off = 0;
     L.header = off;
     off = align256(off + sizeof(PlanHeader));
@@ -199,6 +198,12 @@ WsLayout make_layout(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv
         off = align256(off + sizeof(float) * rows * head_dim);
         L.extra_lse = off;
         off = align256(off + sizeof(float) * rows);
+    }
+    if (prefix_rows > 0) {
+        L.prefix_o = off;
+        off = align256(off + sizeof(float) * static_cast<size_t>(prefix_rows) * head_dim);
+        L.prefix_lse = off;
+        off = align256(off + sizeof(float) * static_cast<size_t>(prefix_rows));
     }
     L.total = off;
     return L;
@@ -294,14 +299,71 @@ int make_maps(StepMaps *m, const void *q, const pa_kv_desc *kv, int tokens, int 
     return rc;
 }
 
+int prefix_plan(int T, int prefix_len, int num_kv_heads, int group, int sms, int *q_tiles,
+                int *nsplit, int *split_keys) {
+    const int tq = q_tile_tokens(group);
+    *q_tiles = (T + tq - 1) / tq;
+    const int tiles = (prefix_len + kLongKeys - 1) / kLongKeys;
+    const int pairs = num_kv_heads * *q_tiles;
+    // the prefix kernel is persistent (one CTA per SM): split the key range so
+    // that every (kv head, query tile, split) item gets an SM of its own
+    int ns = std::max(1, sms / std::max(1, pairs));
+    ns = std::max(1, std::min(ns, std::min(64, tiles)));
+    const int per = std::max(1, (tiles + ns - 1) / ns);  // KV tiles per split (an empty prefix: 1)
+    *split_keys = per * kLongKeys;
+    *nsplit = (prefix_len + *split_keys - 1) / *split_keys;
+    if (*nsplit < 1) *nsplit = 1;
+    return PA_OK;
+}
+
+// Parameters of the shared-prefix ("multi-query") pass: items are (kv head,
+// query tile, key split), implicit in the index; split states go to
+// (split_o, split_lse) at row (pair * nsplit + split) * 128 + r.
+LongParams prefix_params(const pa_kv_desc *kv, const int32_t *prefix_blocks, int32_t prefix_len,
+                         int32_t T, int32_t Hq, float scale, int q_tiles, int nsplit,
+                         int split_keys, float *split_o, float *split_lse, DeviceInfo *dev) {
+    const int group = Hq / kv->num_kv_heads;
+    LongParams lp{};
+    lp.block_tables = prefix_blocks;
+    lp.bt_stride = 0;
+    lp.num_q_tokens = T;
+    lp.num_q_heads = Hq;
+    lp.num_kv_heads = kv->num_kv_heads;
+    lp.group = group;
+    lp.q_tile_tokens = q_tile_tokens(group);
+    lp.block_size = kv->block_size;
+    lp.num_blocks = kv->num_blocks;
+    lp.kv_rows = static_cast<int>(kv_rows(kv));
+    lp.scale_log2 = scale * 1.4426950408889634f;
+    lp.prefix_mode = 1;
+    lp.prefix_len = prefix_len;
+    lp.prefix_nsplit = nsplit;
+    lp.prefix_split_keys = split_keys;
+    lp.prefix_q_tiles = q_tiles;
+    lp.partial_o = split_o;
+    lp.partial_lse = split_lse;
+    lp.status = dev->status;
+    return lp;
+}
+
+// Cascade decode: the shared prefix and where its states and the suffix
+// states live in the workspace.
+struct CascadeArgs {
+    const int32_t *prefix_blocks;
+    int32_t prefix_len;
+    float *prefix_o, *prefix_lse;  // prefix split states
+    float *suffix_o, *suffix_lse;  // suffix state per row, fp32
+};
+
 // Runs the planner, the split-KV kernel and the tensor-core kernel of one
-// step on `s`.  extra_o/extra_lse (cascade prefix state) may be NULL.
+// step on `s`.  With `casc` (cascade decode, all rows short) the step is
+// the unique-suffix pass, run side by side with the shared-prefix pass.
 int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, int32_t max_blocks,
              const int32_t *qsl, const int32_t *ctx, const int32_t *seq_lens, int32_t num_seqs,
              int32_t T, int32_t Hq, float scale, void *out, float *lse, uint8_t *ws,
-             const WsLayout &L, int short_max_rows, int split_keys, const float *extra_o,
-             const float *extra_lse, bool forbid_long, const StepMaps &maps, const Staging &stg,
-             DeviceInfo *dev, cudaStream_t s) {
+             const WsLayout &L, int short_max_rows, int split_keys, const CascadeArgs *casc,
+             bool forbid_long, const StepMaps &maps, const Staging &stg, DeviceInfo *dev,
+             cudaStream_t s) {
     const int D = kv->head_dim;
     const int group = Hq / kv->num_kv_heads;
     const int tq = q_tile_tokens(group);
@@ -376,11 +438,74 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
     sp.counters = pp.counters;
     sp.partial_o = reinterpret_cast<float *>(ws + L.partial_o);
     sp.partial_lse = reinterpret_cast<float *>(ws + L.partial_lse);
-    sp.extra_o = extra_o;
-    sp.extra_lse = extra_lse;
+    sp.out_f32 = nullptr;
     sp.k_scale = fp8 ? kv->k_scale : nullptr;
     sp.v_scale = fp8 ? kv->v_scale : nullptr;
     sp.status = dev->status;
+    sp.num_seqs = num_seqs;
+    sp.num_q_tokens = T;
+    sp.max_items = L.max_short;
+    sp.claim_ahead = kClaimAheadStages;
+
+    if (casc) {
+        // Cascade decode ([AI] §02.1): the shared-prefix pass (tensor cores,
+        // compute-heavy, each prefix tile read once per 128 query rows) and
+        // the unique-suffix pass (split-KV, HBM-bound) have disjoint inputs,
+        // so they run side by side like the two halves of a mixed step: a
+        // first prefix grid on a third of the SMs waits for the plan and lets
+        // the split-KV grid in on the others; a second prefix grid takes SMs
+        // over as split-KV CTAs finish (both pull prefix items from the
+        // step's counter) and completes after both.  The split-KV grid writes
+        // each row's suffix state in fp32; the fold kernel merges it with the
+        // prefix split states into out and lse.
+        int q_tiles, nsplit, split_keys_p;
+        prefix_plan(T, casc->prefix_len, kv->num_kv_heads, group, dev->sms, &q_tiles, &nsplit,
+                    &split_keys_p);
+        LongParams cp = prefix_params(kv, casc->prefix_blocks, casc->prefix_len, T, Hq, scale,
+                                      q_tiles, nsplit, split_keys_p, casc->prefix_o,
+                                      casc->prefix_lse, dev);
+        cp.hdr = hdr;
+        cp.states_only = 1;
+        cp.dynamic = 1;
+        cp.first_done = &hdr->first_done;
+        const int n_prefix = kv->num_kv_heads * q_tiles * nsplit;
+        const int g1 = std::min(std::max(1, dev->sms / 3), n_prefix);
+        LongParams c1 = cp;
+        c1.wait_start = 1;
+        c1.first_ctas = -1;
+        rc = launch_long(c1, maps.q, maps.k, maps.v, D, g1, s);
+        if (rc != PA_OK) return fail(rc, "prefix kernel launch failed: %s",
+                                     cudaGetErrorString(cudaGetLastError()));
+        sp.no_start_wait = 1;
+        sp.out_f32 = casc->suffix_o;
+        sp.lse = casc->suffix_lse;
+        rc = launch_short(sp, maps.k, maps.v, D, false, short_grid, s);
+        if (rc != PA_OK) return fail(rc, "split-KV kernel launch failed: %s",
+                                     cudaGetErrorString(cudaGetLastError()));
+        LongParams c2 = cp;
+        c2.overlap_prev = 1;
+        c2.first_ctas = g1;
+        rc = launch_long(c2, maps.q, maps.k, maps.v, D, n_prefix, s);
+        if (rc != PA_OK) return fail(rc, "prefix kernel launch failed: %s",
+                                     cudaGetErrorString(cudaGetLastError()));
+        PrefixFoldParams f{};
+        f.partial_o = casc->prefix_o;
+        f.partial_lse = casc->prefix_lse;
+        f.extra_o = casc->suffix_o;
+        f.extra_lse = casc->suffix_lse;
+        f.nsplit = nsplit;
+        f.q_tiles = q_tiles;
+        f.pairs = kv->num_kv_heads * q_tiles;
+        f.group = group;
+        f.q_tile_tokens = tq;
+        f.num_q_tokens = T;
+        f.num_q_heads = Hq;
+        f.out = static_cast<__nv_bfloat16 *>(out);
+        f.out_f32 = nullptr;
+        f.lse = lse;
+        rc = launch_prefix_fold(f, D, s);
+        return rc == PA_OK ? PA_OK : fail(rc, "cascade fold launch failed");
+    }
 
     // a long request has q_len * group > short_max_rows, so there are at
     // most T / (short_max_rows / group + 1) of them
@@ -448,6 +573,7 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
         if (rc != PA_OK) return fail(rc, "tensor-core kernel launch failed: %s",
                                      cudaGetErrorString(cudaGetLastError()));
         sp.no_start_wait = 1;
+        sp.claim_ahead = 0;
         rc = launch_short(sp, maps.k, maps.v, D, fp8, short_grid, s);
         if (rc != PA_OK) return fail(rc, "split-KV kernel launch failed: %s",
                                      cudaGetErrorString(cudaGetLastError()));
@@ -501,55 +627,19 @@ int common_checks(const void *q, const pa_kv_desc *kv, int32_t num_q_tokens, int
     return PA_OK;
 }
 
-int prefix_plan(int T, int prefix_len, int num_kv_heads, int group, int sms, int *q_tiles,
-                int *nsplit, int *split_keys) {
-    const int tq = q_tile_tokens(group);
-    *q_tiles = (T + tq - 1) / tq;
-    const int tiles = (prefix_len + kLongKeys - 1) / kLongKeys;
-    const int pairs = num_kv_heads * *q_tiles;
-    // the prefix kernel is persistent (one CTA per SM): split the key range so
-    // that every (kv head, query tile, split) item gets an SM of its own
-    int ns = std::max(1, sms / std::max(1, pairs));
-    ns = std::max(1, std::min(ns, std::min(64, tiles)));
-    const int per = (tiles + ns - 1) / ns;  // KV tiles per split
-    *split_keys = per * kLongKeys;
-    *nsplit = (prefix_len + *split_keys - 1) / *split_keys;
-    if (*nsplit < 1) *nsplit = 1;
-    return PA_OK;
-}
-
 int run_prefix(const void *q, const pa_kv_desc *kv, const int32_t *prefix_blocks, int32_t prefix_len,
-               int32_t T, int32_t Hq, float scale, void *out, float *out_f32, float *lse,
-               uint8_t *ws, const WsLayout &L, const StepMaps &maps, DeviceInfo *dev,
-               cudaStream_t s) {
+               int32_t T, int32_t Hq, float scale, void *out, float *lse, uint8_t *ws,
+               const WsLayout &L, const StepMaps &maps, DeviceInfo *dev, cudaStream_t s) {
     const int group = Hq / kv->num_kv_heads;
     int q_tiles, nsplit, split_keys;
     prefix_plan(T, prefix_len, kv->num_kv_heads, group, dev->sms, &q_tiles, &nsplit, &split_keys);
-    LongParams lp{};
-    lp.out = static_cast<__nv_bfloat16 *>(out);
-    lp.lse = lse;
-    lp.out_f32 = out_f32;
-    lp.block_tables = prefix_blocks;
-    lp.bt_stride = 0;
-    lp.num_q_tokens = T;
-    lp.num_q_heads = Hq;
-    lp.num_kv_heads = kv->num_kv_heads;
-    lp.group = group;
-    lp.q_tile_tokens = q_tile_tokens(group);
-    lp.block_size = kv->block_size;
-    lp.num_blocks = kv->num_blocks;
-    lp.kv_rows = static_cast<int>(kv_rows(kv));
-    lp.scale_log2 = scale * 1.4426950408889634f;
-    lp.prefix_mode = 1;
-    lp.prefix_len = prefix_len;
-    lp.prefix_nsplit = nsplit;
-    lp.prefix_split_keys = split_keys;
-    lp.prefix_q_tiles = q_tiles;
     // a split prefix leaves its split states to the fold kernel, which runs
     // the fold of a (kv head, query tile) on many SMs
-    lp.partial_o = reinterpret_cast<float *>(ws + L.partial_o);
-    lp.partial_lse = reinterpret_cast<float *>(ws + L.partial_lse);
-    lp.status = dev->status;
+    LongParams lp = prefix_params(kv, prefix_blocks, prefix_len, T, Hq, scale, q_tiles, nsplit,
+                                  split_keys, reinterpret_cast<float *>(ws + L.prefix_o),
+                                  reinterpret_cast<float *>(ws + L.prefix_lse), dev);
+    lp.out = static_cast<__nv_bfloat16 *>(out);
+    lp.lse = lse;
     const int grid = kv->num_kv_heads * q_tiles * nsplit;
     int rc = launch_long(lp, maps.q, maps.k, maps.v, kv->head_dim, grid, s);
     if (rc != PA_OK) return fail(rc, "prefix kernel launch failed");
@@ -565,7 +655,6 @@ int run_prefix(const void *q, const pa_kv_desc *kv, const int32_t *prefix_blocks
         f.num_q_tokens = T;
         f.num_q_heads = Hq;
         f.out = static_cast<__nv_bfloat16 *>(out);
-        f.out_f32 = out_f32;
         f.lse = lse;
         rc = launch_prefix_fold(f, kv->head_dim, s);
         if (rc != PA_OK) return fail(rc, "prefix fold launch failed");
@@ -640,8 +729,8 @@ int attention_in_fixed_workspace(const void *q, const pa_kv_desc *kv,
     if ((rc = make_maps(&maps, q, kv, num_q_tokens, num_q_heads)) != PA_OK) return rc;
     return run_step(q, kv, block_tables, max_blocks_per_seq, query_start_loc, context_lens,
                     seq_lens, num_seqs, num_q_tokens, num_q_heads, scale, out, lse,
-                    static_cast<uint8_t *>(scratch), L, kShortMaxRows, 0, nullptr, nullptr,
-                    false, maps, Staging(), dev, s);
+                    static_cast<uint8_t *>(scratch), L, kShortMaxRows, 0, nullptr, false, maps,
+                    Staging(), dev, s);
 }
 
 int set_error_message(int code, const char *msg) { return fail(code, "%s", msg); }
@@ -728,7 +817,7 @@ int pa_attention_ex(const void *q, const pa_kv_desc *kv, const int32_t *block_ta
                     seq_lens, num_seqs, num_q_tokens, num_q_heads, scale, out, lse,
                     static_cast<uint8_t *>(workspace), L,
                     short_q_max_rows < 0 ? kShortMaxRows : short_q_max_rows, split_keys, nullptr,
-                    nullptr, false, maps, stg, dev, static_cast<cudaStream_t>(stream));
+                    false, maps, stg, dev, static_cast<cudaStream_t>(stream));
 }
 
 size_t pa_fp8_staging_bytes(int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
@@ -800,7 +889,7 @@ int pa_prefix_attention(const void *q, const pa_kv_desc *kv, const int32_t *pref
     StepMaps maps;
     if ((rc = make_maps(&maps, q, kv, num_q_tokens, num_q_heads)) != PA_OK) return rc;
     return run_prefix(q, kv, prefix_blocks, prefix_len, num_q_tokens, num_q_heads, scale, out,
-                      nullptr, lse, static_cast<uint8_t *>(workspace), L, maps, dev,
+                      lse, static_cast<uint8_t *>(workspace), L, maps, dev,
                       static_cast<cudaStream_t>(stream));
 }
 
@@ -838,15 +927,17 @@ int pa_cascade_decode(const void *q, const pa_kv_desc *kv, const int32_t *prefix
     StepMaps maps;
     if ((rc = make_maps(&maps, q, kv, num_q_tokens, num_q_heads)) != PA_OK) return rc;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    float *xo = reinterpret_cast<float *>(ws + L.extra_o);
-    float *xl = reinterpret_cast<float *>(ws + L.extra_lse);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    rc = run_prefix(q, kv, prefix_blocks, prefix_len, num_q_tokens, num_q_heads, scale, nullptr, xo,
-                    xl, ws, L, maps, dev, s);
-    if (rc != PA_OK) return rc;
+    CascadeArgs casc;
+    casc.prefix_blocks = prefix_blocks;
+    casc.prefix_len = prefix_len;
+    casc.prefix_o = reinterpret_cast<float *>(ws + L.prefix_o);
+    casc.prefix_lse = reinterpret_cast<float *>(ws + L.prefix_lse);
+    casc.suffix_o = reinterpret_cast<float *>(ws + L.extra_o);
+    casc.suffix_lse = reinterpret_cast<float *>(ws + L.extra_lse);
     return run_step(q, kv, block_tables, max_blocks_per_seq, query_start_loc, context_lens,
                     seq_lens, num_seqs, num_q_tokens, num_q_heads, scale, out, lse, ws, L,
-                    kShortMaxRows, 0, xo, xl, true, maps, Staging(), dev, s);
+                    kShortMaxRows, 0, &casc, true, maps, Staging(), dev,
+                    static_cast<cudaStream_t>(stream));
 }
 
 int pa_validate_metadata(const int32_t *block_tables, int32_t max_blocks_per_seq,

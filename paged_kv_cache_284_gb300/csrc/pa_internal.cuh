@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <utility>
 
 #include "../../include/pa.h"
@@ -38,6 +39,10 @@ constexpr int kMinSplitStages = 4;    // 256 keys: smallest automatic split
 // and a fold).
 constexpr int kSplitItemsPerCta = 3;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
+// split-KV kernel: a CTA claims its next work item this many ring stages
+// before its current one ends (enough to hide the claim and the prefetch of
+// the item's record and first block ids)
+constexpr int kClaimAheadStages = 3;
 
 // Work list written by the plan kernel into the caller's workspace.
 struct PlanHeader {
@@ -104,6 +109,7 @@ __device__ __forceinline__ void store_record(T *base, int rec, const T &r) {
 // Byte offsets of the workspace regions (same computation on host and device).
 struct WsLayout {
     size_t header, counters, short_items, long_items, partial_o, partial_lse, extra_o, extra_lse;
+    size_t prefix_o, prefix_lse;    // cascade prefix pass: split states [rows][D], [rows]
     size_t stage_base, stage_list;  // fp8 staging bookkeeping ([num_seqs] each)
     size_t total;
     int max_short, max_long, cap_rows, num_counters;
@@ -123,10 +129,17 @@ struct ShortParams {
     const ShortItem *items;
     int *counters;
     float *partial_o, *partial_lse;
-    const float *extra_o, *extra_lse;  // cascade: prefix state folded into the output
+    // if set, every row's final state is written as fp32 (o normalised
+    // [row][D], lse [row] into `lse`) instead of bf16 out: cascade decode's
+    // suffix state, merged with the prefix state by the fold kernel (bf16
+    // pools only)
+    float *out_f32;
     const float *k_scale, *v_scale;    // fp8 pool: per-kv-head dequantisation scales
     int no_start_wait;  // launched after the step's first tensor-core grid (see LongParams)
     unsigned *status;
+    int num_seqs, num_q_tokens;  // sizes of the metadata arrays and of q (L2 warm-up)
+    int max_items;               // work-record capacity of the workspace (>= 1)
+    int claim_ahead;  // ring stages before an item's end at which the next is claimed (0: at its start)
 };
 
 struct LongParams {
@@ -141,6 +154,7 @@ struct LongParams {
     float scale_log2;
     int prefix_mode;  // 1: non-causal shared prefix, items implicit
     int prefix_len, prefix_nsplit, prefix_split_keys, prefix_q_tiles;
+    int states_only;  // 1: every item writes its split state, even when unsplit
     PlanHeader *hdr;
     const LongItem *items;
     float *partial_o, *partial_lse;
@@ -194,6 +208,9 @@ struct PlanParams {
 // ((h * q_tiles + qt) * nsplit + s) * 128 + r.
 struct PrefixFoldParams {
     const float *partial_o, *partial_lse;
+    // optional further state per row ([T*Hq][D] fp32 normalised, [T*Hq] lse):
+    // cascade decode's suffix state
+    const float *extra_o, *extra_lse;
     int nsplit, q_tiles, pairs, group, q_tile_tokens, num_q_tokens, num_q_heads;
     __nv_bfloat16 *out;  // bf16 result, or
     float *out_f32;      // fp32 result (a state for the suffix pass)
@@ -220,6 +237,25 @@ struct PdlLaunch {
     PdlLaunch(const PdlLaunch &) = delete;
     PdlLaunch &operator=(const PdlLaunch &) = delete;
 };
+
+// Runs fn() (a cudaError_t-returning set-up step such as a function
+// attribute) once per device: attributes set with cudaFuncSetAttribute belong
+// to the function's instance on the device current at the call, so a second
+// GPU in the same process needs its own.
+struct PerDeviceOnce {
+    std::mutex mu;
+    uint64_t mask = 0;  // bit d: done on device d (devices 0..63)
+};
+template <typename F>
+int once_per_device(PerDeviceOnce &once, F &&fn) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(once.mu);
+    if ((once.mask >> dev) & 1u) return PA_OK;
+    if (fn() != cudaSuccess) return PA_ERR_CUDA;
+    once.mask |= 1ull << dev;
+    return PA_OK;
+}
 
 // Every kernel launch of the library goes through launch_kernel, which keeps
 // the process-wide count that pa_kernel_launches() reports.
@@ -384,6 +420,25 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *tm, in
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
         : "memory");
 }
+// L2 prefetch of slice `part` of `parts` of [base, base + bytes) by the 32
+// lanes of a warp, in bulk pieces of at most 4 KB.  Only whole 16-byte units
+// inside the range are named (the bulk prefetch needs 16-byte alignment).
+// A prefetch is a hint: it moves nothing into registers or shared memory.
+__device__ __forceinline__ void l2_prefetch_slice(const void *base, size_t bytes, int part,
+                                                  int parts, int lane) {
+    const uint64_t lo = (reinterpret_cast<uint64_t>(base) + 15) & ~15ull;
+    const uint64_t hi = (reinterpret_cast<uint64_t>(base) + bytes) & ~15ull;
+    if (!base || hi <= lo || parts <= 0) return;
+    const uint64_t per = (((hi - lo) + parts - 1) / parts + 15) & ~15ull;
+    const uint64_t s = lo + per * static_cast<uint64_t>(part);
+    if (s >= hi) return;
+    const uint64_t e = s + per < hi ? s + per : hi;
+    for (uint64_t a = s + static_cast<uint64_t>(lane) * 4096; a < e; a += 32 * 4096) {
+        const uint32_t n = static_cast<uint32_t>(e - a < 4096 ? e - a : 4096);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(n) : "memory");
+    }
+}
+
 // Order this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA / tensor core) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {

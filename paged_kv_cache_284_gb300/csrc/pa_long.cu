@@ -689,7 +689,7 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
             const int tok = it.tok0 + ttok;
             const int hq = it.h * p.group + jh;
             const int64_t orow = static_cast<int64_t>(tok) * p.num_q_heads + hq;
-            const bool direct = it.nsplit == 1;
+            const bool direct = it.nsplit == 1 && !p.states_only;
             const int64_t prow = static_cast<int64_t>(it.partial_base + it.split * kLongRows + r);
             for (int qd = 0; qd < D / 64; ++qd) {
                 const int col = o0 + qd * 32;
@@ -769,6 +769,9 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
 // (kv head, query tile), its lanes across the head dimension, so that all
 // splits' loads of a row are in flight at once and the work spreads over
 // many SMs (one CTA per 8 rows).  A split count of at most 64 is assumed.
+// With f.extra_o set, one more state per row (cascade decode's unique-suffix
+// state) joins the merge: the prefix and suffix halves of cascade inference
+// meet here, in one epilogue.
 template <int D>
 __global__ void __launch_bounds__(256) prefix_fold_kernel(const PrefixFoldParams f) {
     pdl_wait();  // the prefix pass's states
@@ -786,18 +789,26 @@ __global__ void __launch_bounds__(256) prefix_fold_kernel(const PrefixFoldParams
     const float l0 = lane < ns ? __ldcg(f.partial_lse + base + lane * kLongRows) : -INFINITY;
     const float l1 = lane + 32 < ns ? __ldcg(f.partial_lse + base + (lane + 32) * kLongRows)
                                     : -INFINITY;
-    float M = fmaxf(l0, l1);
+    const int64_t row = static_cast<int64_t>(tok) * f.num_q_heads + h * f.group + jh;
+    const float xl = f.extra_o ? __ldcg(f.extra_lse + row) : -INFINITY;
+    float M = fmaxf(fmaxf(l0, l1), xl);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float w0 = (lane < ns && M != -INFINITY) ? __expf(l0 - M) : 0.f;
     const float w1 = (lane + 32 < ns && M != -INFINITY) ? __expf(l1 - M) : 0.f;
+    const float wx = (xl != -INFINITY) ? __expf(xl - M) : 0.f;
     float wsum = w0 + w1;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    wsum += wx;
     const bool col = lane < D / 4;  // this lane's float4 of the row
     const float4 *po = reinterpret_cast<const float4 *>(f.partial_o + base * D) + (col ? lane : 0);
     const int64_t stride = static_cast<int64_t>(kLongRows) * (D / 4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (wx > 0.f && col) {
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(f.extra_o + row * D) + lane);
+        acc = make_float4(wx * v.x, wx * v.y, wx * v.z, wx * v.w);
+    }
     for (int s0 = 0; s0 < ns; s0 += 8) {
         float ws[8];
         float4 v[8];
@@ -818,7 +829,6 @@ __global__ void __launch_bounds__(256) prefix_fold_kernel(const PrefixFoldParams
         }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    const int64_t row = static_cast<int64_t>(tok) * f.num_q_heads + h * f.group + jh;
     if (col) {
         const float4 a = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         if (f.out_f32) {
@@ -849,14 +859,11 @@ size_t long_smem_bytes(int head_dim) {
 
 template <int D>
 static int configure_long() {
-    static bool done = false;
-    if (!done) {
-        if (cudaFuncSetAttribute(long_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 LongGeom<D>::kSmemBytes) != cudaSuccess)
-            return PA_ERR_CUDA;
-        done = true;
-    }
-    return PA_OK;
+    static PerDeviceOnce once;
+    return once_per_device(once, [] {
+        return cudaFuncSetAttribute(long_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    LongGeom<D>::kSmemBytes);
+    });
 }
 
 // grid: the caller passes an upper bound on the number of items; the kernel is

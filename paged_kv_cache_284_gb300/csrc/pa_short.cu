@@ -20,8 +20,9 @@
 //  * split-KV: a long sequence is cut into several items; each writes a
 //    partial (o, lse) state, and the last item to finish (device counter)
 //    folds them with the merge operator (2048ai.net page on the vLLM V1
-//    engine, §02.1 级联推理) -- the fused split-KV epilogue.  A cascade prefix
-//    state can be folded in the same epilogue.
+//    engine, §02.1 级联推理) -- the fused split-KV epilogue.  For cascade
+//    decode the final state of each row is written in fp32 instead, for the
+//    fold that merges it with the shared-prefix state.
 //  * FP8 pool (same page, §02 推理优化: KV-cache quantisation): K and V are
 //    e4m3 codes, one 16-key x 128-dim TMA box per chunk (half the bytes of
 //    bf16), 8 chunks (128 keys) per ring stage.  The MMAs run in f16: e4m3 decodes exactly to f16, q is
@@ -71,10 +72,22 @@ struct ShortGeom {
 struct StageMeta {
     int item, stage, flags, pad;
 };
+// What the consumers need of a work item, handed over by the producer in
+// shared memory with the item's first stage (the producer has already
+// loaded the record and the request's query start and context), so that an
+// item starts without a chain of dependent global loads in the consumers.
+struct ItemInfo {
+    int b, h, split, nsplit;
+    int counter, partial_base, q_begin, q_count;
+    int seq_len, stage_end, tok0, ctx;
+};
 constexpr int kFirst = 1, kLast = 2;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: lazy max update
 constexpr int kFoldBatch = 8;              // splits loaded together by the fold
+// q is warmed into L2 before the plan completes only when it is this small
+// (decode-sized steps); a large step's q mostly feeds the tensor-core kernel
+constexpr size_t kPrefetchQMaxBytes = 4u << 20;
 
 __device__ __forceinline__ float quad_max(float v) {
     v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
@@ -127,6 +140,24 @@ __device__ __forceinline__ int chunk_row_of(const ShortParams &p, const ShortIte
         blk = min(max(blk, 0), p.num_blocks - 1);
     }
     return (blk * p.num_kv_heads + h) * p.block_size + key0 % p.block_size;
+}
+
+// L1 prefetch of an item's query rows (q_count tokens x the group's heads,
+// each token's group one contiguous run of group * D bf16), by the producer
+// lanes right after the item's first stage is issued: the consumers load
+// them as mma fragments when that stage lands, and find them in L1.
+template <int D>
+__device__ __forceinline__ void prefetch_item_q(const ShortParams &p, int tok0, int h,
+                                                int q_count, int lane) {
+    const int seg = p.group * D * 2;     // bytes of one token's group
+    const int lines = (seg + 127) / 128 + 1;  // a run may straddle one more line
+    for (int i = lane; i < q_count * lines; i += 32) {
+        const int t = i / lines, l = i - t * lines;
+        const char *run = reinterpret_cast<const char *>(
+            p.q + (static_cast<int64_t>(tok0 + t) * p.num_q_heads + h * p.group) * D);
+        const char *a = run + min(l * 128, seg - 1);
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
+    }
 }
 
 // Work item idx: its record and kv head.
@@ -279,8 +310,8 @@ __device__ __forceinline__ void swapped_chunks(Consumer<D> &cs, const uint32_t (
 
 // Item epilogue of a swapped fp8 item: row sums over the 8 lanes of a row,
 // the 4 consumer warps merged through the stage buffer, then warp 0 writes
-// rows 2t and 2t+1 (output or partial state).  A cascade prefix state is
-// never folded here: cascade calls take bf16 pools only.
+// rows 2t and 2t+1 (output or partial state).  Cascade calls take bf16 pools
+// only, so the fp32 state output is not needed here.
 template <int D>
 __device__ __forceinline__ void swapped_epilogue(Consumer<D> &cs, const ShortParams &p,
                                                  float *scratch, int lane, int warp) {
@@ -381,6 +412,9 @@ __global__ void __launch_bounds__(kShortThreads, 2)
     uint64_t *empty = full + kStages;
     StageMeta *meta = reinterpret_cast<StageMeta *>(empty + kStages);
     int *ctl = reinterpret_cast<int *>(meta + kStages);
+    ItemInfo *info = reinterpret_cast<ItemInfo *>(ctl + 16);
+    static_assert(kStages * (8 + 8 + 16) + 64 + kStages * sizeof(ItemInfo) <= G::kCtlBytes,
+                  "control area");
     volatile int *abort_flag = ctl;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -393,9 +427,25 @@ __global__ void __launch_bounds__(kShortThreads, 2)
         ctl[1] = 0;
         fence_mbar_init();
     }
-    if (warp == kShortConsumerWarps && lane == 0) {
-        tma_prefetch_desc(&tmk);
-        tma_prefetch_desc(&tmv);
+    if (warp == kShortConsumerWarps) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+        }
+        // Warm L2 with this CTA's slice of the step's metadata (and of q when
+        // it is small) while the plan is still running: the first items' block
+        // ids and query rows are then L2 hits.  A prefetch is only a hint and
+        // reads nothing into registers, so it may run before the wait below.
+        const int part = blockIdx.x, parts = gridDim.x;
+        l2_prefetch_slice(p.block_tables,
+                          static_cast<size_t>(p.num_seqs) * p.bt_stride * sizeof(int), part,
+                          parts, lane);
+        const size_t q_bytes = static_cast<size_t>(p.num_q_tokens) * p.num_q_heads * D * 2;
+        if (q_bytes <= kPrefetchQMaxBytes) l2_prefetch_slice(p.q, q_bytes, part, parts, lane);
+        if (part == 0) {
+            l2_prefetch_slice(p.qsl, (p.num_seqs + 1) * sizeof(int), 0, 1, lane);
+            l2_prefetch_slice(p.ctx, p.num_seqs * sizeof(int), 0, 1, lane);
+        }
     }
     __syncthreads();
     // everything below reads the plan's output; after the step's first
@@ -417,26 +467,29 @@ __global__ void __launch_bounds__(kShortThreads, 2)
         // ============================ producer ============================
         uint32_t it = 0;
         bool aborted = false;
-        // The next item's index, descriptor, length and first block ids are
-        // fetched one step per stage while the current item is still being
-        // issued, and block ids are read one 8-stage batch ahead, so the ring
-        // never waits on a chain of dependent global loads.  When the grid
-        // starts at once (it waited for the plan), CTA c starts with item c;
-        // beside a tensor-core grid, CTAs start as SMs free up and every item
-        // comes from the counter, so the longest items go to the CTAs that
-        // start first.
+        // The next item's index, record, first block ids, query start and
+        // context are fetched one dependent step per stage while the current
+        // item is still being issued (the steps are taken while the ring is
+        // full, or all at the item's last stage), and block ids are read one
+        // 8-stage batch ahead, so the ring never waits on a chain of dependent
+        // global loads.  When the grid starts at once (it waited for the
+        // plan), CTA c starts with item c; beside a tensor-core grid, CTAs
+        // start as SMs free up and every item comes from the counter, so the
+        // longest items go to the CTAs that start first.
         const int first_static = p.no_start_wait ? 0 : static_cast<int>(gridDim.x);
         int cur_idx = blockIdx.x;
         if (p.no_start_wait) {
             if (lane == 0) cur_idx = atomicAdd(&p.hdr->short_next, 1);
             cur_idx = __shfl_sync(0xffffffffu, cur_idx, 0);
         }
-        ShortItem cur{};
-        int cur_h = 0, cur_L = 0, cur_row = -1;
+        int cur_h = 0, cur_row = -1, cur_q0 = 0, cur_ctx = 0;
+        // the record is loaded together with the item count (records up to
+        // max_items exist in the workspace, valid or not)
+        ShortItem cur = short_work(p, min(cur_idx, p.max_items - 1), cur_h);
         if (cur_idx < num_items) {
-            cur = short_work(p, cur_idx, cur_h);
-            cur_L = cur.seq_len;
-            cur_row = chunk_row_of(p, cur, cur_h, cur_L, cur.stage_begin, lane);
+            cur_row = chunk_row_of(p, cur, cur_h, cur.seq_len, cur.stage_begin, lane);
+            cur_q0 = __ldg(p.qsl + cur.b);
+            cur_ctx = __ldg(p.ctx + cur.b);
         }
         while (!aborted) {
             if (cur_idx >= num_items) {
@@ -453,21 +506,51 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                 __syncwarp();
                 break;
             }
-            int nxt_idx = 0;
-            if (lane == 0)  // read two stages later
-                nxt_idx = atomicAdd(&p.hdr->short_next, 1) + first_static;
             ShortItem nxt{};
-            int nxt_h = 0, nxt_L = 0, nxt_row = -1, pf = 0;  // prefetch state of the next item
+            // prefetch state of the next item
+            int nxt_idx = 0, nxt_h = 0, nxt_row = -1, nxt_q0 = 0, nxt_ctx = 0, pf = 0;
             const int nst = cur.stage_end - cur.stage_begin;  // planner stages
             const int nrs = (nst + G::kPSR - 1) / G::kPSR;     // ring stages
+            // The next item is claimed from the counter p.claim_ahead stages
+            // before this one ends, so that items go out longest first in the
+            // order the CTAs free up (a claim at the item's start would tie a
+            // CTA with a long item to a long next item as well); the
+            // remaining stages cover the claim's and the prefetch's latency.
+            // Beside a mixed step's tensor-core grids the claim is made at
+            // the item's start (claim_ahead = 0): there the ragged end of
+            // this grid hands SMs to the tensor-core work sooner, measured
+            // 1 % faster per step.
+            const int rel_claim = p.claim_ahead > 0 ? max(0, nrs - p.claim_ahead) : 0;
             int batch_row = cur_row, next_batch = -1;
             for (int rel = 0; rel < nrs; ++rel, ++it) {
                 const int st = cur.stage_begin + rel * G::kPSR;  // its first planner stage
                 if (rel % G::kRSB == 0) {
                     if (rel > 0) batch_row = next_batch;
                     next_batch = (rel + G::kRSB < nrs)
-                                     ? chunk_row_of(p, cur, cur_h, cur_L, st + 8, lane)
+                                     ? chunk_row_of(p, cur, cur_h, cur.seq_len, st + 8, lane)
                                      : -1;
+                }
+                if (rel == rel_claim && lane == 0)
+                    nxt_idx = atomicAdd(&p.hdr->short_next, 1) + first_static;
+                // one prefetch step for the next item per stage after the
+                // claim, before this stage's slot is awaited (from the ring's
+                // first reuse on); every remaining step at the item's last stage
+                for (;;) {
+                    if (pf >= 2 || !((it >= kStages && rel > rel_claim) || rel == nrs - 1)) break;
+                    if (pf == 0) {
+                        nxt_idx = __shfl_sync(0xffffffffu, nxt_idx, 0);
+                        nxt = short_work(p, min(nxt_idx, p.max_items - 1), nxt_h);
+                        pf = 1;
+                    } else {
+                        if (nxt_idx < num_items) {
+                            nxt_row = chunk_row_of(p, nxt, nxt_h, nxt.seq_len, nxt.stage_begin,
+                                                   lane);
+                            nxt_q0 = __ldg(p.qsl + nxt.b);
+                            nxt_ctx = __ldg(p.ctx + nxt.b);
+                        }
+                        pf = 2;
+                    }
+                    if (rel != nrs - 1) break;
                 }
                 // lane c < kCPS takes the row of chunk c of this stage
                 const int crow = __shfl_sync(0xffffffffu, batch_row,
@@ -489,6 +572,22 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                     mm.flags = (rel == 0 ? kFirst : 0) | (rel == nrs - 1 ? kLast : 0);
                     mm.pad = 0;
                     meta[slot] = mm;
+                    if (rel == 0) {
+                        ItemInfo ii;
+                        ii.b = cur.b;
+                        ii.h = cur_h;
+                        ii.split = cur.split;
+                        ii.nsplit = cur.nsplit;
+                        ii.counter = cur.counter;
+                        ii.partial_base = cur.partial_base;
+                        ii.q_begin = cur.q_begin;
+                        ii.q_count = cur.q_count;
+                        ii.seq_len = cur.seq_len;
+                        ii.stage_end = cur.stage_end;
+                        ii.tok0 = cur_q0;
+                        ii.ctx = cur_ctx;
+                        info[slot] = ii;
+                    }
                     mbar_arrive_expect_tx(&full[slot],
                                           static_cast<uint32_t>(nvalid * 2 * G::kChunkBytes));
                 }
@@ -501,32 +600,16 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                         tma_load_2d(v_box(slot, lane, hf), &tmv, hf * 64, crow, &full[slot]);
                     }
                 }
+                if (rel == 0) prefetch_item_q<D>(p, cur_q0 + cur.q_begin, cur_h, cur.q_count, lane);
                 __syncwarp();
-                // one prefetch step per stage from the third stage on; the last
-                // stage finishes whatever is left
-                for (;;) {
-                    if (pf == 0 && (rel >= 2 || rel == nrs - 1)) {
-                        nxt_idx = __shfl_sync(0xffffffffu, nxt_idx, 0);
-                        if (nxt_idx < num_items) nxt = short_work(p, nxt_idx, nxt_h);
-                        pf = 1;
-                    } else if (pf == 1 && (rel >= 3 || rel == nrs - 1)) {
-                        if (nxt_idx < num_items) {
-                            nxt_L = nxt.seq_len;
-                            nxt_row = chunk_row_of(p, nxt, nxt_h, nxt_L, nxt.stage_begin, lane);
-                        }
-                        pf = 2;
-                    } else {
-                        break;
-                    }
-                    if (rel != nrs - 1) break;
-                }
             }
             if (aborted) break;
             cur_idx = nxt_idx;
             cur = nxt;
             cur_h = nxt_h;
-            cur_L = nxt_L;
             cur_row = nxt_row;
+            cur_q0 = nxt_q0;
+            cur_ctx = nxt_ctx;
         }
         if (aborted && lane == 0) {
             flag_status(p.status, PA_DEV_WAIT_TIMEOUT);
@@ -553,9 +636,9 @@ __global__ void __launch_bounds__(kShortThreads, 2)
         if (mm.item < 0) break;
 
         if (mm.flags & kFirst) {
-            // ---- item setup ----
-            int item_h;
-            const ShortItem item = short_work(p, mm.item, item_h);
+            // ---- item setup (the producer's copy of the record) ----
+            const ItemInfo item = info[slot];
+            const int item_h = item.h;
             cs.b = item.b;
             cs.h = item_h;
             cs.split = item.split;
@@ -563,9 +646,9 @@ __global__ void __launch_bounds__(kShortThreads, 2)
             cs.counter = item.counter * p.num_kv_heads + item_h;
             // a piece of a request: its tokens start q_begin tokens in, so its
             // rows' causal limits start q_begin keys further
-            cs.tok0 = __ldg(p.qsl + item.b) + item.q_begin;
+            cs.tok0 = item.tok0 + item.q_begin;
             const int n = item.q_count;
-            cs.ctx = __ldg(p.ctx + item.b) + item.q_begin;
+            cs.ctx = item.ctx + item.q_begin;
             const int L = item.seq_len;
             cs.key_end = min(item.stage_end * kStageKeys, L);
             cs.R = n * p.group;
@@ -914,40 +997,25 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                         const int hq = cs.h * p.group + r % p.group;
                         const int64_t row = static_cast<int64_t>(tok) * p.num_q_heads + hq;
                         if (cs.nsplit == 1) {
-                            float wa = 1.f, wb = 0.f, lse_f = lse_v;
-                            const float *xo = nullptr;
-                            if (p.extra_o) {
-                                const float xl = __ldg(p.extra_lse + row);
-                                const float M = fmaxf(lse_v, xl);
-                                if (M == -INFINITY) {
-                                    wa = 0.f;
-                                } else {
-                                    const float ea = __expf(lse_v - M), eb = __expf(xl - M);
-                                    wa = ea / (ea + eb);
-                                    wb = eb / (ea + eb);
-                                    lse_f = M + __logf(ea + eb);
-                                    xo = p.extra_o + row * D;
-                                }
-                            }
-                            uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + row * D);
+                            if (p.out_f32) {
+                                float *dst = p.out_f32 + row * D;
     #pragma unroll
-                            for (int pi = 0; pi < NT; ++pi) {
-                                float x, y;
-                                const int col = pair_of(pi, half, x, y);
-                                x *= inv;
-                                y *= inv;
-                                if (p.extra_o) {
-                                    x *= wa;
-                                    y *= wa;
-                                    if (xo) {
-                                        const float2 e2 = __ldg(reinterpret_cast<const float2 *>(xo + col));
-                                        x += wb * e2.x;
-                                        y += wb * e2.y;
-                                    }
+                                for (int pi = 0; pi < NT; ++pi) {
+                                    float x, y;
+                                    const int col = pair_of(pi, half, x, y);
+                                    __stcg(reinterpret_cast<float2 *>(dst + col),
+                                           make_float2(x * inv, y * inv));
                                 }
-                                dst[col >> 1] = pack_bf16x2(x, y);
+                            } else {
+                                uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + row * D);
+    #pragma unroll
+                                for (int pi = 0; pi < NT; ++pi) {
+                                    float x, y;
+                                    const int col = pair_of(pi, half, x, y);
+                                    dst[col >> 1] = pack_bf16x2(x * inv, y * inv);
+                                }
                             }
-                            if (p.lse && t == 0) p.lse[row] = lse_f;
+                            if (p.lse && t == 0) p.lse[row] = lse_v;
                         } else {
                             float *dst = p.partial_o + static_cast<int64_t>(cs.partial_base + r) * D;
     #pragma unroll
@@ -978,14 +1046,13 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                         const int tok = cs.tok0 + r / p.group;
                         const int hq = cs.h * p.group + r % p.group;
                         const int64_t row = static_cast<int64_t>(tok) * p.num_q_heads + hq;
-                        const float xl = p.extra_o ? __ldg(p.extra_lse + row) : -INFINITY;
                         const float *pl = p.partial_lse + base + r;
                         const float4 *po = reinterpret_cast<const float4 *>(
                                                p.partial_o + static_cast<int64_t>(base + r) * D) + e4;
                         const int64_t ostride = static_cast<int64_t>(cs.R) * (D / 4);
                         // splits are read kFoldBatch at a time so their L2
                         // round trips overlap
-                        float M = xl;
+                        float M = -INFINITY;
                         for (int s0 = 0; s0 < cs.nsplit; s0 += kFoldBatch) {
 #pragma unroll
                             for (int j = 0; j < kFoldBatch; ++j)
@@ -1014,21 +1081,18 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                                     acc.w += w * v[j].w;
                                 }
                             }
-                            if (p.extra_o) {
-                                const float w = __expf(xl - M);
-                                const float4 v = __ldg(reinterpret_cast<const float4 *>(p.extra_o + row * D) + e4);
-                                wsum += w;
-                                acc.x += w * v.x;
-                                acc.y += w * v.y;
-                                acc.z += w * v.z;
-                                acc.w += w * v.w;
-                            }
                         }
                         const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-                        uint2 pk2;
-                        pk2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-                        pk2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-                        reinterpret_cast<uint2 *>(p.out + row * D)[e4] = pk2;
+                        if (p.out_f32) {
+                            __stcg(reinterpret_cast<float4 *>(p.out_f32 + row * D) + e4,
+                                   make_float4(acc.x * inv, acc.y * inv, acc.z * inv,
+                                               acc.w * inv));
+                        } else {
+                            uint2 pk2;
+                            pk2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+                            pk2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+                            reinterpret_cast<uint2 *>(p.out + row * D)[e4] = pk2;
+                        }
                         if (e4 == 0 && p.lse) p.lse[row] = wsum > 0.f ? M + __logf(wsum) : -INFINITY;
                     }
                 }
@@ -1048,14 +1112,12 @@ size_t short_smem_bytes(int head_dim) {
 
 template <int D, bool FP8>
 static int configure_short() {
-    static bool done = false;  // per process; attribute is per function, device-independent
-    if (!done) {
-        if (cudaFuncSetAttribute(short_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 ShortGeom<D, FP8>::kSmemBytes) != cudaSuccess)
-            return PA_ERR_CUDA;
-        done = true;
-    }
-    return PA_OK;
+    static PerDeviceOnce once;
+    return once_per_device(once, [] {
+        return cudaFuncSetAttribute(short_kernel<D, FP8>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    ShortGeom<D, FP8>::kSmemBytes);
+    });
 }
 
 template <int D, bool FP8>
