@@ -145,8 +145,13 @@ size_t pa_fp8_staging_bytes(int32_t num_kv_heads, int32_t head_dim, int32_t bloc
 /*
  * Varlen paged attention for one continuous-batching step ([TC], [CH]).
  * Request b owns query tokens [qsl[b], qsl[b+1]) (qsl = query_start_loc,
- * int32 [num_seqs+1], qsl[0] = 0, non-decreasing, qsl[num_seqs] =
- * num_q_tokens).  context_lens[b] tokens of it are already cached;
+ * int32 [num_seqs+1], qsl[0] = 0, non-decreasing, qsl[num_seqs] <=
+ * num_q_tokens; query rows from qsl[num_seqs] on belong to no request and
+ * out / lse there are left untouched -- so one CUDA graph captured at
+ * num_seqs requests and num_q_tokens tokens serves any smaller batch padded
+ * with empty requests: q_len 0, context 0, seq_len 0, table row naming any
+ * valid block; the padding tokens get slot -1 in pa_write_kv).
+ * context_lens[b] tokens of it are already cached;
  * seq_lens[b] = context_lens[b] + q_len (int32 [num_seqs] each).  Its keys
  * 0..seq_lens[b]-1 live in the physical blocks block_tables[b][0..] (int32
  * [num_seqs][max_blocks_per_seq]; entries past ceil(seq_len/bs) are never
@@ -268,7 +273,8 @@ int pa_cascade_decode(const void *q, const pa_kv_desc *kv, const int32_t *prefix
 
 /*
  * Host-side check of step metadata (HOST pointers): qsl[0] == 0, qsl
- * non-decreasing and ending at num_q_tokens, seq_lens == context_lens + q_len,
+ * non-decreasing and ending at or below num_q_tokens, seq_lens ==
+ * context_lens + q_len,
  * every block id a request reads within [0, num_blocks), and (if
  * slot_mapping is not NULL) every slot either negative or inside the pool
  * and no slot used twice.  Returns PA_OK or PA_ERR_BAD_METADATA (with a
@@ -301,6 +307,44 @@ const char *pa_status_string(int code);
 enum { PA_KERNEL_WRITE_KV = 0, PA_KERNEL_PLAN = 1, PA_KERNEL_SPLIT_KV = 2,
        PA_KERNEL_TENSOR_CORE = 3 };
 int pa_set_profile_events(int32_t which, void *start_event, void *end_event);
+
+/*
+ * Test hook for the bounded device waits (no counterpart on the pages).
+ * Every wait inside the kernels -- on a pipeline barrier, or the wait of a
+ * step's last tensor-core grid for the CTAs of its first -- gives up after
+ * 2 s, raises PA_DEV_WAIT_TIMEOUT, lets its copies in flight land and
+ * returns; the context stays usable.  This hook makes one such wait run
+ * out on purpose, so a test can check that path.  Nothing faults or traps.
+ *   PA_TEST_STALL_NONE        normal operation (the default)
+ *   PA_TEST_STALL_SPLIT_KV    in every later split-KV launch that waits for
+ *                             its plan (not the mixed step's side-by-side
+ *                             launch), CTA 0's producer stops after its
+ *                             first stage: CTA 0's consumers wait for a
+ *                             stage that never comes, time out and return.
+ *                             The step's result is then incomplete.
+ *   PA_TEST_STALL_LAST_GRID   in every later side-by-side step (split-KV
+ *                             and tensor-core kernels together), the last
+ *                             tensor-core grid waits for one CTA more than
+ *                             the first grid launched.  All work is done
+ *                             and the result is right; only the wait times
+ *                             out.
+ * Process-wide, read at launch time; set it from one thread, with no call
+ * of this library in flight on the host.
+ */
+enum { PA_TEST_STALL_NONE = 0, PA_TEST_STALL_SPLIT_KV = 1, PA_TEST_STALL_LAST_GRID = 2 };
+int pa_set_test_stall(int32_t which);
+
+/*
+ * Work counter of the tensor-core kernel (a check of its causal tile
+ * skipping; "vLLM中如何实现大模型推理加速技术？", chunked prefill: a chunk's
+ * score block covers only the keys up to its last row, 16^2*6 rather than
+ * 16^2*9 for 48 tokens in 16-token tiles).  While `counter` (a DEVICE
+ * pointer to one uint64) is set, every later launch of the tensor-core
+ * kernel adds to it the number of 128-key tiles for which it issued Q K^T,
+ * summed over its items (128-row query tile, kv head).  NULL (the default)
+ * turns it off.  Process-wide; for tests, not for timed runs.
+ */
+int pa_set_tile_counter(uint64_t *counter);
 
 /*
  * Read (and, if clear != 0, reset) the PA_DEV_* status word of the current

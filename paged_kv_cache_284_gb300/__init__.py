@@ -41,6 +41,7 @@ EXPORTED = ["pa_write_kv", "pa_attention_workspace_size", "pa_attention", "pa_at
             "pa_bm_fork", "pa_bm_schedule", "pa_bm_free_request", "pa_bm_num_free_blocks",
             "pa_bm_num_cached_blocks", "pa_bm_block_ref_count", "pa_bm_request_blocks",
             "pa_bm_num_computed",
+            "pa_set_test_stall", "pa_set_tile_counter",
             # request router for sharded replicas (include/pa_shard.h)
             "pa_partition_requests"]
 PA_KERNEL_WRITE_KV, PA_KERNEL_PLAN, PA_KERNEL_SPLIT_KV, PA_KERNEL_TENSOR_CORE = range(4)
@@ -106,6 +107,8 @@ def _declare(lib):
         "pa_bm_request_blocks": ([P, i64, P, i32], i32),
         "pa_bm_num_computed": ([P, i64], i32),
         "pa_partition_requests": ([P, i32, i32, P, P], ctypes.c_int),
+        "pa_set_test_stall": ([i32], ctypes.c_int),
+        "pa_set_tile_counter": ([P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -329,6 +332,22 @@ def partition_requests(seq_lens, num_ranks: int):
     if rc != PA_OK:
         raise PaError(rc, "pa_partition_requests", "bad sizes or a negative length")
     return rank_of.tolist(), loads[:int(num_ranks)].tolist()
+
+
+PA_TEST_STALL_NONE, PA_TEST_STALL_SPLIT_KV, PA_TEST_STALL_LAST_GRID = 0, 1, 2
+
+
+def set_test_stall(which: int):
+    """Test hook: make one bounded device wait run out (see pa.h)."""
+    _check(lib().pa_set_test_stall(int(which)), "pa_set_test_stall")
+
+
+def set_tile_counter(counter=None):
+    """Count the tensor-core kernel's 128-key tiles into `counter` (a CUDA
+    int64 tensor of one element) until called with None."""
+    if counter is not None and (counter.dtype != torch.int64 or not counter.is_cuda):
+        raise TypeError("counter must be a CUDA int64 tensor")
+    _check(lib().pa_set_tile_counter(_ptr(counter)), "pa_set_tile_counter")
 
 
 def read_device_status(clear: bool = True, stream=None) -> int:

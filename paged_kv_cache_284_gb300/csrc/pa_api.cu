@@ -117,6 +117,8 @@ int make_q_map(CUtensorMap *m, const void *q, int tokens, int heads, int head_di
 }
 
 std::atomic<unsigned long long> g_launches{0};
+std::atomic<int> g_test_stall{PA_TEST_STALL_NONE};  // pa_set_test_stall
+std::atomic<uint64_t *> g_tile_counter{nullptr};     // pa_set_tile_counter
 
 // Profiling hook state (pa_set_profile_events).
 void *g_prof[4][2] = {};
@@ -446,6 +448,8 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
     sp.num_q_tokens = T;
     sp.max_items = L.max_short;
     sp.claim_ahead = kClaimAheadStages;
+    const int stall = g_test_stall.load(std::memory_order_relaxed);
+    sp.test_stall = stall == PA_TEST_STALL_SPLIT_KV ? 1 : 0;
 
     if (casc) {
         // Cascade decode ([AI] §02.1): the shared-prefix pass (tensor cores,
@@ -477,6 +481,7 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
         if (rc != PA_OK) return fail(rc, "prefix kernel launch failed: %s",
                                      cudaGetErrorString(cudaGetLastError()));
         sp.no_start_wait = 1;
+        sp.test_stall = 0;
         sp.out_f32 = casc->suffix_o;
         sp.lse = casc->suffix_lse;
         rc = launch_short(sp, maps.k, maps.v, D, false, short_grid, s);
@@ -538,6 +543,8 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
         lp.partial_o = sp.partial_o;
         lp.partial_lse = sp.partial_lse;
         lp.status = dev->status;
+        lp.tile_counter = reinterpret_cast<unsigned long long *>(
+            g_tile_counter.load(std::memory_order_relaxed));
         if (staged) {
             lp.stage_base = pp.stage_base;
             lp.k_scale = kv->k_scale;
@@ -574,6 +581,7 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
                                      cudaGetErrorString(cudaGetLastError()));
         sp.no_start_wait = 1;
         sp.claim_ahead = 0;
+        sp.test_stall = 0;
         rc = launch_short(sp, maps.k, maps.v, D, fp8, short_grid, s);
         if (rc != PA_OK) return fail(rc, "split-KV kernel launch failed: %s",
                                      cudaGetErrorString(cudaGetLastError()));
@@ -581,7 +589,8 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
         l2.dynamic = 1;
         l2.overlap_prev = 1;
         l2.first_done = &hdr->first_done;
-        l2.first_ctas = g1;
+        // the test hook waits for one CTA that the first grid never had
+        l2.first_ctas = g1 + (stall == PA_TEST_STALL_LAST_GRID ? 1 : 0);
         rc = launch_long(l2, maps.q, lk, lv, D, long_grid, s);
         if (rc != PA_OK) return fail(rc, "tensor-core kernel launch failed: %s",
                                      cudaGetErrorString(cudaGetLastError()));
@@ -969,8 +978,8 @@ int pa_validate_metadata(const int32_t *block_tables, int32_t max_blocks_per_seq
                             (long long)j, blk);
         }
     }
-    if (num_seqs > 0 && query_start_loc[num_seqs] != num_q_tokens)
-        return fail(PA_ERR_BAD_METADATA, "query_start_loc[num_seqs] = %d != num_q_tokens %d",
+    if (num_seqs > 0 && query_start_loc[num_seqs] > num_q_tokens)
+        return fail(PA_ERR_BAD_METADATA, "query_start_loc[num_seqs] = %d > num_q_tokens %d",
                     query_start_loc[num_seqs], num_q_tokens);
     if (slot_mapping && num_q_tokens > 0) {
         const int64_t nslots = static_cast<int64_t>(num_blocks) * block_size;
@@ -995,6 +1004,23 @@ int pa_set_profile_events(int32_t which, void *start_event, void *end_event) {
     std::lock_guard<std::mutex> lock(g_prof_mu);
     g_prof[which][0] = start_event;
     g_prof[which][1] = end_event;
+    return PA_OK;
+}
+
+int pa_set_tile_counter(uint64_t *counter) {
+    g_err[0] = 0;
+    if (counter && !aligned(counter, 8))
+        return fail(PA_ERR_INVALID_ARG, "tile counter must be 8-byte aligned");
+    g_tile_counter.store(counter, std::memory_order_relaxed);
+    return PA_OK;
+}
+
+int pa_set_test_stall(int32_t which) {
+    g_err[0] = 0;
+    if (which != PA_TEST_STALL_NONE && which != PA_TEST_STALL_SPLIT_KV &&
+        which != PA_TEST_STALL_LAST_GRID)
+        return fail(PA_ERR_INVALID_ARG, "unknown test stall %d", which);
+    g_test_stall.store(which, std::memory_order_relaxed);
     return PA_OK;
 }
 

@@ -32,6 +32,7 @@ constexpr int kLongRows = 128;        // tcgen05 tile: M = 128 query rows
 constexpr int kLongKeys = 128;        // tcgen05 tile: N = 128 keys per KV tile
 constexpr int kLongThreads = 384;     // 12 warps: K+Q loads, QK^T, 8 x softmax, V loads, PV
 constexpr int kPlanThreads = 1024;
+constexpr int kSmallPlanSeqs = 16;    // steps of at most this many requests plan on one warp
 constexpr int kMinSplitStages = 4;    // 256 keys: smallest automatic split
 // Automatic split size: total split-KV stages / (this x persistent CTAs).  The
 // items are taken longest first, so a request is cut only when it is long
@@ -140,6 +141,7 @@ struct ShortParams {
     int num_seqs, num_q_tokens;  // sizes of the metadata arrays and of q (L2 warm-up)
     int max_items;               // work-record capacity of the workspace (>= 1)
     int claim_ahead;  // ring stages before an item's end at which the next is claimed (0: at its start)
+    int test_stall;   // test hook: CTA 0's producer stops after its first stage
 };
 
 struct LongParams {
@@ -174,6 +176,7 @@ struct LongParams {
     int dynamic, wait_start;
     int *first_done;
     int first_ctas;
+    unsigned long long *tile_counter;  // if set: += 128-key tiles whose Q K^T was issued
     // 1: launched as a programmatic dependent of the split-KV kernel of the
     // same step.  The kernel then reads nothing but the plan's output (and
     // the step's inputs) before its last instruction, where it waits for the

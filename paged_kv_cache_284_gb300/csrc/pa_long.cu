@@ -422,7 +422,8 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                 const Item it = decode_item(p, idx);
                 if (it.nt == 0) continue;
                 if (!mbar_wait(&bars->q_full, k_item & 1, abort_flag)) { ok = false; break; }
-                for (int j = 0; j < it.nt; ++j) {
+                int j = 0;
+                for (; j < it.nt; ++j) {
                     const uint32_t tt = t + j;
                     const int ks = tt % kKStages;
                     const int sb = tt & 1;
@@ -445,6 +446,7 @@ __global__ void __launch_bounds__(32 * kLongWarps, 1)
                     tc_commit(&bars->s_full[sb]);
                     if (j == it.nt - 1) tc_commit(&bars->q_empty);
                 }
+                if (p.tile_counter) atomicAdd(p.tile_counter, static_cast<unsigned long long>(j));
                 t += it.nt;
                 ++k_item;
             }

@@ -15,7 +15,8 @@
 
 namespace pa {
 
-// Exclusive block-wide prefix sum over kPlanThreads threads.
+// Exclusive block-wide prefix sum over the kT threads of the block.
+template <int kT>
 __device__ int block_exclusive_scan(int v, int *tmp, int *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = v;
@@ -27,7 +28,7 @@ __device__ int block_exclusive_scan(int v, int *tmp, int *total) {
     if (lane == 31) tmp[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int w = (lane < (kPlanThreads / 32)) ? tmp[lane] : 0;
+        int w = (lane < (kT / 32)) ? tmp[lane] : 0;
         int wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -59,7 +60,7 @@ __device__ __forceinline__ long long warp_sum_ll(long long x) {
 // Block-wide sums of N non-negative 64-bit values and the maximum of one
 // non-negative int, all in one pass (two barriers for the lot).
 constexpr int kRedStride = kPlanThreads / 32 + 1;
-template <int N>
+template <int kT, int N>
 __device__ void block_reduce(long long (&v)[N], int &mx, long long *tmp) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -72,7 +73,7 @@ __device__ void block_reduce(long long (&v)[N], int &mx, long long *tmp) {
     }
     __syncthreads();
     if (warp == 0) {
-        const bool in = lane < kPlanThreads / 32;
+        const bool in = lane < kT / 32;
 #pragma unroll
         for (int i = 0; i < N; ++i) {
             const long long w = warp_sum_ll(in ? tmp[i * kRedStride + lane] : 0);
@@ -90,6 +91,7 @@ __device__ void block_reduce(long long (&v)[N], int &mx, long long *tmp) {
 }
 
 // Exclusive block-wide prefix sums of two values at once (tmp: 66 ints).
+template <int kT>
 __device__ void block_exclusive_scan2(int a, int b, int *tmp, int &pa, int &pb, int &ta, int &tb) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int ia = a, ib = b;
@@ -108,7 +110,7 @@ __device__ void block_exclusive_scan2(int a, int b, int *tmp, int &pa, int &pb, 
     }
     __syncthreads();
     if (warp == 0) {
-        const bool in = lane < kPlanThreads / 32;
+        const bool in = lane < kT / 32;
         const int wa = in ? tmp[lane] : 0, wb = in ? tmp[33 + lane] : 0;
         int sa = wa, sb = wb;
 #pragma unroll
@@ -135,10 +137,11 @@ __device__ void block_exclusive_scan2(int a, int b, int *tmp, int &pa, int &pb, 
     __syncthreads();
 }
 
+template <int kT>
 __device__ long long block_sum_ll(long long v, long long *tmp) {
     long long a[1] = {v};
     int m = 0;
-    block_reduce<1>(a, m, tmp);
+    block_reduce<kT, 1>(a, m, tmp);
     return a[0];
 }
 
@@ -186,20 +189,25 @@ __device__ __forceinline__ Piece piece_of(const PlanParams &p, const ReqInfo &r,
     return pc;
 }
 
-constexpr int kSortBins = kPlanThreads;  // bins of the longest-first sort
-
-// Sort bin of query tile qt of a long request: bin 0 holds the most 128-key
-// tiles.
-__device__ __forceinline__ int long_bin(const PlanParams &p, const ReqInfo &r, int qt) {
-    const int nvalid = min(p.q_tile_tokens, r.n - qt * p.q_tile_tokens);
-    const int kend = min(r.len, r.ctx + qt * p.q_tile_tokens + nvalid);
-    const int tiles = (kend + kLongKeys - 1) / kLongKeys;
-    return kSortBins - 1 - min(tiles, kSortBins - 1);
+// The longest-first sorts are counting sorts with one bin per thread (kT
+// bins); a bin holds 2^shift consecutive lengths, the least shift that fits
+// the step's longest item, so a small plan still sorts long items closely.
+__device__ __forceinline__ int bin_shift(int longest, int bins) {
+    int sh = 0;
+    while ((longest >> sh) >= bins) ++sh;
+    return sh;
 }
 
-// Sort bin of a split-KV item of `stages` stages: bin 0 holds the longest.
-__device__ __forceinline__ int short_bin(int stages) {
-    return kSortBins - 1 - min(stages, kSortBins - 1);
+// 128-key tiles of query tile qt of a long request.
+__device__ __forceinline__ int long_tiles(const PlanParams &p, const ReqInfo &r, int qt) {
+    const int nvalid = min(p.q_tile_tokens, r.n - qt * p.q_tile_tokens);
+    const int kend = min(r.len, r.ctx + qt * p.q_tile_tokens + nvalid);
+    return (kend + kLongKeys - 1) / kLongKeys;
+}
+
+// Sort bin of an item of `len` stages (or tiles): bin 0 holds the longest.
+__device__ __forceinline__ int len_bin(int len, int shift, int bins) {
+    return bins - 1 - min(len >> shift, bins - 1);
 }
 
 // A piece of `stages` stages cut into ns splits whose ranges differ by at
@@ -215,7 +223,11 @@ __device__ __forceinline__ SplitCut split_cut(int stages, int sp) {
     return c;
 }
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
+// kT threads: 1024 in general, one warp for steps of few requests (its
+// phases then cost shuffles instead of block barriers).
+template <int kT>
+__global__ void __launch_bounds__(kT) plan_kernel(PlanParams p) {
+    constexpr int kSortBins = kT;
     __shared__ int tmp[66];
     __shared__ long long tmpl[5 * kRedStride];
     __shared__ int bins[kSortBins];
@@ -226,14 +238,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     pdl_wait();
     pdl_trigger();
     if (tid == 0) s_overflow = 0;
-    for (int i = tid; i < kSortBins; i += kPlanThreads) bins[i] = 0;
+    for (int i = tid; i < kSortBins; i += kT) bins[i] = 0;
     // 0. fp8 pool with a staging area: long requests get consecutive bf16
     // staging blocks in request order while they fit (a request that does
     // not fit, and every later one, runs as split-KV pieces instead).
     int staged = 0, staged_blocks = 0;
     if (p.fp8 && p.stage_cap > 0) {
         int cand_base = 0;
-        for (int b0 = 0; b0 < p.num_seqs; b0 += kPlanThreads) {
+        for (int b0 = 0; b0 < p.num_seqs; b0 += kT) {
             const int b = b0 + tid;
             int cnt = 0;
             if (b < p.num_seqs) {
@@ -242,19 +254,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
                     cnt = (len + p.block_size - 1) / p.block_size;
             }
             int tot_c, tot_s;
-            const int base = cand_base + block_exclusive_scan(cnt, tmp, &tot_c);
+            const int base = cand_base + block_exclusive_scan<kT>(cnt, tmp, &tot_c);
             const bool fits = cnt > 0 && base + cnt <= p.stage_cap;
-            const int idx = staged + block_exclusive_scan(fits ? 1 : 0, tmp, &tot_s);
+            const int idx = staged + block_exclusive_scan<kT>(fits ? 1 : 0, tmp, &tot_s);
             if (b < p.num_seqs) p.stage_base[b] = fits ? base : -1;
             if (fits) p.stage_list[idx] = b;
-            staged_blocks += static_cast<int>(block_sum_ll(fits ? cnt : 0, tmpl));
+            staged_blocks += static_cast<int>(block_sum_ll<kT>(fits ? cnt : 0, tmpl));
             cand_base += tot_c;
             staged += tot_s;
         }
         __syncthreads();
     }
     // Request tid's metadata is read once and kept in registers; only steps
-    // with more than kPlanThreads requests read the others again per pass.
+    // with more than kT requests read the others again per pass.
     const ReqInfo mine = tid < p.num_seqs ? load_req(p, tid) : ReqInfo{};
     auto req = [&](int b) { return b == tid ? mine : load_req(p, b); };
     __syncthreads();
@@ -262,7 +274,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     // 1. totals: split-KV work (in stages), pieces, longest piece, query tiles
     long long tot[3] = {0, 0, 0};  // work, pieces, tensor-core query tiles
     int max_stages = 0;
-    for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+    for (int b = tid; b < p.num_seqs; b += kT) {
         const ReqInfo r = req(b);
         for (int i = 0; i < r.pieces; ++i) {
             const Piece pc = piece_of(p, r, i);
@@ -272,7 +284,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         tot[1] += r.pieces;
         tot[2] += r.qtiles;
     }
-    block_reduce<3>(tot, max_stages, tmpl);
+    block_reduce<kT, 3>(tot, max_stages, tmpl);
     const long long total_work = tot[0] * hkv;
     const long long total_pieces = tot[1];
     const long long total_qtiles = tot[2];
@@ -314,7 +326,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         sp_a = sp_b = max(sp_t, min(sp_k, cap));
     }
     long long cnt[4] = {0, 0, 0, 0};  // items and partial-state rows at sp_a, at sp_b
-    for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+    for (int b = tid; b < p.num_seqs; b += kT) {
         const ReqInfo r = req(b);
         for (int i = 0; i < r.pieces; ++i) {
             const Piece pc = piece_of(p, r, i);
@@ -327,7 +339,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     }
     {
         int unused = 0;
-        block_reduce<4>(cnt, unused, tmpl);
+        block_reduce<kT, 4>(cnt, unused, tmpl);
     }
     const bool one_round = p.split_stages <= 0 && W > 0 && P <= C;
     const bool use_a = !one_round || cnt[0] * hkv <= C;
@@ -337,7 +349,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         if ((items <= p.max_short && rows <= p.cap_rows) || sp >= max_stages) break;
         sp *= 2;
         long long c2[2] = {0, 0};
-        for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+        for (int b = tid; b < p.num_seqs; b += kT) {
             const ReqInfo r = req(b);
             for (int i = 0; i < r.pieces; ++i) {
                 const Piece pc = piece_of(p, r, i);
@@ -347,11 +359,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
             }
         }
         int unused = 0;
-        block_reduce<2>(c2, unused, tmpl);
+        block_reduce<kT, 2>(c2, unused, tmpl);
         items = c2[0] * hkv;
         rows = c2[1] * hkv;
     }
     if (tid == 0 && total_pieces * hkv > p.num_counters) s_overflow = 1;
+    // no split-KV item is longer than sp stages or than the longest piece
+    const int shift_s = bin_shift(min(sp, max_stages), kSortBins);
 
     int short_base = 0, long_base = 0, row_base = 0, piece_base = 0;
 
@@ -360,24 +374,24 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     // consecutive slots of their bin, reserved with one atomic.  Partial-state
     // rows and completion counters are handed out in request order by block
     // scans.
-    for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+    for (int b = tid; b < p.num_seqs; b += kT) {
         const ReqInfo r = req(b);
         for (int i = 0; i < r.pieces; ++i) {
             const SplitCut c = split_cut(piece_of(p, r, i).stages, sp);
-            if (c.rem > 0) atomicAdd(&bins[short_bin(c.q + 1)], c.rem);
-            if (c.ns > c.rem) atomicAdd(&bins[short_bin(c.q)], c.ns - c.rem);
+            if (c.rem > 0) atomicAdd(&bins[len_bin(c.q + 1, shift_s, kSortBins)], c.rem);
+            if (c.ns > c.rem) atomicAdd(&bins[len_bin(c.q, shift_s, kSortBins)], c.ns - c.rem);
         }
     }
     __syncthreads();
     {
         int tot_s;
         const int v = tid < kSortBins ? bins[tid] : 0;
-        const int off = block_exclusive_scan(v, tmp, &tot_s);
+        const int off = block_exclusive_scan<kT>(v, tmp, &tot_s);
         if (tid < kSortBins) bins[tid] = off;
         short_base = tot_s;  // records
         __syncthreads();
     }
-    for (int b0 = 0; b0 < p.num_seqs; b0 += kPlanThreads) {
+    for (int b0 = 0; b0 < p.num_seqs; b0 += kT) {
         const int b = b0 + tid;
         ReqInfo r{};
         if (b < p.num_seqs) r = req(b);
@@ -388,7 +402,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
             if (ns > 1) n_rows += ns * pc.q_count * p.group * hkv;
         }
         int off_r, off_p, tot_r, tot_p;
-        block_exclusive_scan2(n_rows, r.pieces, tmp, off_r, off_p, tot_r, tot_p);
+        block_exclusive_scan2<kT>(n_rows, r.pieces, tmp, off_r, off_p, tot_r, tot_p);
         off_r += row_base;
         off_p += piece_base;
         row_base += tot_r;
@@ -403,8 +417,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
             const Piece pc = piece_of(p, r, i);
             const SplitCut c = split_cut(pc.stages, sp);
             const int R = pc.q_count * p.group;
-            const int slot_hi = c.rem > 0 ? atomicAdd(&bins[short_bin(c.q + 1)], c.rem) : 0;
-            const int slot_lo = c.ns > c.rem ? atomicAdd(&bins[short_bin(c.q)], c.ns - c.rem) : 0;
+            const int slot_hi =
+                c.rem > 0 ? atomicAdd(&bins[len_bin(c.q + 1, shift_s, kSortBins)], c.rem) : 0;
+            const int slot_lo =
+                c.ns > c.rem ? atomicAdd(&bins[len_bin(c.q, shift_s, kSortBins)], c.ns - c.rem)
+                             : 0;
             ShortItem it;
             it.b = b;
             it.nsplit = c.ns;
@@ -430,19 +447,29 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     // number of 128-key tiles), so persistent CTAs that take items in order
     // finish together.
     if (total_qtiles > 0) {
-        for (int i = tid; i < kSortBins; i += kPlanThreads) bins[i] = 0;
-        __syncthreads();
-        for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+        for (int i = tid; i < kSortBins; i += kT) bins[i] = 0;
+        // the longest tensor-core item: a request's last query tile
+        int max_tiles = 0;
+        for (int b = tid; b < p.num_seqs; b += kT) {
+            const ReqInfo r = req(b);
+            if (r.qtiles > 0) max_tiles = max(max_tiles, long_tiles(p, r, r.qtiles - 1));
+        }
+        {
+            long long unused[1] = {0};
+            block_reduce<kT, 1>(unused, max_tiles, tmpl);
+        }
+        const int shift_l = bin_shift(max_tiles, kSortBins);
+        for (int b = tid; b < p.num_seqs; b += kT) {
             const ReqInfo r = req(b);
             for (int qt = 0; qt < r.qtiles; ++qt)
-                atomicAdd(&bins[long_bin(p, r, qt)], 1);
+                atomicAdd(&bins[len_bin(long_tiles(p, r, qt), shift_l, kSortBins)], 1);
         }
         __syncthreads();
         {
             // one bin per thread: exclusive scan gives each bin's first slot
             int tot_l;
             const int v = tid < kSortBins ? bins[tid] : 0;
-            const int off = block_exclusive_scan(v, tmp, &tot_l);
+            const int off = block_exclusive_scan<kT>(v, tmp, &tot_l);
             if (tid < kSortBins) bins[tid] = off;
             long_base = tot_l;
             __syncthreads();
@@ -450,7 +477,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         if (static_cast<long long>(long_base) * hkv > p.max_long) {
             if (tid == 0) s_overflow = 1;
         } else {
-            for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+            for (int b = tid; b < p.num_seqs; b += kT) {
                 const ReqInfo r = req(b);
                 for (int qt = 0; qt < r.qtiles; ++qt) {
                     const int nvalid = min(p.q_tile_tokens, r.n - qt * p.q_tile_tokens);
@@ -459,14 +486,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
                     it.q_tile = qt;
                     it.key_begin = 0;
                     it.key_end = min(r.len, r.ctx + qt * p.q_tile_tokens + nvalid);
-                    store_record(p.long_items, atomicAdd(&bins[long_bin(p, r, qt)], 1), it);
+                    store_record(p.long_items,
+                                 atomicAdd(&bins[len_bin(long_tiles(p, r, qt), shift_l,
+                                                         kSortBins)], 1),
+                                 it);
                 }
             }
         }
     }
 
     // 4. counters and header ----------------------------------------------------
-    for (int i = tid; i < p.num_counters; i += kPlanThreads) p.counters[i] = 0;
+    for (int i = tid; i < p.num_counters; i += kT) p.counters[i] = 0;
     __syncthreads();
     if (tid == 0) {
         // A work list that did not fit is never run partially: no items at all.
@@ -484,8 +514,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
 }
 
 int launch_plan(const PlanParams &p, cudaStream_t s) {
+    if (p.num_seqs <= kSmallPlanSeqs) {
+        PdlLaunch l(1, 32, 0, s);
+        return launch_kernel(l, plan_kernel<32>, p) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
     PdlLaunch l(1, kPlanThreads, 0, s);
-    return launch_kernel(l, plan_kernel, p) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return launch_kernel(l, plan_kernel<kPlanThreads>, p) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace pa

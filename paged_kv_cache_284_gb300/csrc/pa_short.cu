@@ -561,6 +561,9 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                 if (lane == 0 && it >= kStages)
                     ok = mbar_wait(&empty[slot], ((it / kStages) - 1) & 1, abort_flag);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
+                // test hook: stop after the first stage, as a producer would
+                // whose wait had run out
+                if (p.test_stall && blockIdx.x == 0 && it == 1) ok = 0;
                 if (!ok) {
                     aborted = true;
                     break;

@@ -34,6 +34,11 @@ def test_library_exports_every_declared_function():
     assert set(names) == set(pk.EXPORTED)
 
 
+def test_test_stall_hook_rejects_unknown_values():
+    assert pk.lib().pa_set_test_stall(7) == pk.PA_ERR_INVALID_ARG
+    assert pk.lib().pa_set_test_stall(pk.PA_TEST_STALL_NONE) == pk.PA_OK
+
+
 def test_status_strings():
     assert pk.lib().pa_status_string(0) == b"PA_OK"
     assert pk.lib().pa_status_string(3) == b"PA_ERR_WORKSPACE"

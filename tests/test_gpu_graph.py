@@ -3,6 +3,8 @@ replayed on new metadata.  Planning runs on the device, so nothing the host
 passes depends on the metadata's contents: a graph captured for one step of
 a given shape serves every later step of that shape, with the inputs copied
 into the captured buffers in place."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -86,4 +88,65 @@ def test_graph_replay_on_new_metadata():
     g.replay()
     torch.cuda.synchronize()
     assert np.array_equal(bits(st.out), bits(eager_out))
+    assert_status_clean()
+
+
+def padded(step, n_seqs, n_tokens):
+    """`step` padded to n_seqs requests and n_tokens tokens: the extra
+    requests are empty (q_len 0, context 0, seq_len 0, table rows naming
+    block 0) and the extra tokens belong to no request (slot -1: nothing is
+    written for them)."""
+    T, B = step.num_q_tokens, step.num_seqs
+
+    def grow(t, n, fill=0):
+        out = torch.full((n,) + tuple(t.shape[1:]), fill, dtype=t.dtype)
+        out[:t.shape[0]] = t
+        return out
+
+    bt = torch.zeros((n_seqs, step.block_tables.shape[1]), dtype=torch.int32)
+    bt[:B] = step.block_tables
+    qsl = torch.full((n_seqs + 1,), T, dtype=torch.int32)
+    qsl[:B + 1] = step.query_start_loc
+    return dataclasses.replace(
+        step, q=grow(step.q, n_tokens), k=grow(step.k, n_tokens), v=grow(step.v, n_tokens),
+        slot_mapping=grow(step.slot_mapping, n_tokens, -1), block_tables=bt,
+        query_start_loc=qsl, context_lens=grow(step.context_lens, n_seqs),
+        seq_lens=grow(step.seq_lens, n_seqs))
+
+
+def test_one_graph_serves_every_decode_batch_up_to_its_size():
+    """One write + attention step captured at 64 decode requests replays
+    batches of 1, 7, 33 and 64 rows: each smaller batch is padded with empty
+    requests, and each replay is compared with the oracle on that batch; the
+    padding rows of out are left untouched."""
+    N = 64
+    pool, (full,) = workloads.decode_heavy(seed=284095, num_seqs=N, lo=16, hi=1500,
+                                           num_q_heads=8, num_kv_heads=2)
+    kc, vc = pool.k_cache.to(DEV), pool.v_cache.to(DEV)
+    st = StaticStep(full, kc, vc)
+    st.run()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        st.run()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st.run()
+    torch.cuda.synchronize()
+    kb, vb = oracle_write(full, bits(pool.k_cache), bits(pool.v_cache))
+    for b in (1, 7, 33, N):
+        step = workloads.subset(full, range(b))
+        st.load(padded(step, N, N))
+        st.out.fill_(float("nan"))
+        st.lse.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        T = step.num_q_tokens
+        ref_o, ref_l = oracle_attend(step, kb, vb)
+        assert_attention_close(st.out[:T], st.lse[:T], ref_o, ref_l, f"graph replay, batch {b}")
+        assert torch.isnan(st.out[T:].float()).all() and torch.isnan(st.lse[T:]).all()
+    assert np.array_equal(bits(kc), kb) and np.array_equal(bits(vc), vb)
     assert_status_clean()
