@@ -120,25 +120,34 @@ struct Consumer {
     float m0, m1, l0, l1;
 };
 
-// TMA row coordinate (cache row = (block, kv head h, offset)) of chunk
-// first_stage*4 + lane of a split-KV item -- one lane per chunk of an
-// 8-stage batch -- or -1 past the item's keys.  Out-of-range table columns
-// and block ids are clamped and flagged.
-__device__ __forceinline__ int chunk_row_of(const ShortParams &p, const ShortItem &item, int h,
-                                            int L, int first_stage, int lane) {
+// Block-table entry of chunk first_stage*4 + lane of a split-KV item -- one
+// lane per chunk of an 8-stage batch -- loaded raw; *has = false past the
+// item's keys.  The TMA row is computed from it by chunk_row_from, later, so
+// that the load's latency overlaps the stages issued in between.  An
+// out-of-range table column is clamped and flagged.
+__device__ __forceinline__ int chunk_blk_load(const ShortParams &p, const ShortItem &item, int L,
+                                              int first_stage, int lane, bool &has) {
     const int key_end = min(item.stage_end * kStageKeys, L);
     const int key0 = (first_stage * kStageChunks + lane) * kChunkKeys;
-    if (key0 >= key_end) return -1;
+    has = key0 < key_end;
+    if (!has) return 0;
     int col = key0 / p.block_size;
     if (col >= p.bt_stride) {  // seq_len beyond the table row
         flag_status(p.status, PA_DEV_BAD_METADATA);
         col = p.bt_stride - 1;
     }
-    int blk = __ldg(p.block_tables + static_cast<int64_t>(item.b) * p.bt_stride + col);
+    return __ldg(p.block_tables + static_cast<int64_t>(item.b) * p.bt_stride + col);
+}
+// TMA row coordinate (cache row = (block, kv head h, offset)) of that chunk,
+// or -1 without one; an out-of-range block id is clamped and flagged.
+__device__ __forceinline__ int chunk_row_from(const ShortParams &p, int blk, bool has, int h,
+                                              int first_stage, int lane) {
+    if (!has) return -1;
     if (blk < 0 || blk >= p.num_blocks) {
         flag_status(p.status, PA_DEV_BAD_BLOCK);
         blk = min(max(blk, 0), p.num_blocks - 1);
     }
+    const int key0 = (first_stage * kStageChunks + lane) * kChunkKeys;
     return (blk * p.num_kv_heads + h) * p.block_size + key0 % p.block_size;
 }
 
@@ -487,9 +496,11 @@ __global__ void __launch_bounds__(kShortThreads, 2)
         // max_items exist in the workspace, valid or not)
         ShortItem cur = short_work(p, min(cur_idx, p.max_items - 1), cur_h);
         if (cur_idx < num_items) {
-            cur_row = chunk_row_of(p, cur, cur_h, cur.seq_len, cur.stage_begin, lane);
+            bool has;
+            const int blk = chunk_blk_load(p, cur, cur.seq_len, cur.stage_begin, lane, has);
             cur_q0 = __ldg(p.qsl + cur.b);
             cur_ctx = __ldg(p.ctx + cur.b);
+            cur_row = chunk_row_from(p, blk, has, cur_h, cur.stage_begin, lane);
         }
         while (!aborted) {
             if (cur_idx >= num_items) {
@@ -508,7 +519,8 @@ __global__ void __launch_bounds__(kShortThreads, 2)
             }
             ShortItem nxt{};
             // prefetch state of the next item
-            int nxt_idx = 0, nxt_h = 0, nxt_row = -1, nxt_q0 = 0, nxt_ctx = 0, pf = 0;
+            int nxt_idx = 0, nxt_h = 0, nxt_blk = 0, nxt_q0 = 0, nxt_ctx = 0, pf = 0;
+            bool nxt_has = false;
             const int nst = cur.stage_end - cur.stage_begin;  // planner stages
             const int nrs = (nst + G::kPSR - 1) / G::kPSR;     // ring stages
             // The next item is claimed from the counter p.claim_ahead stages
@@ -521,14 +533,17 @@ __global__ void __launch_bounds__(kShortThreads, 2)
             // this grid hands SMs to the tensor-core work sooner, measured
             // 1 % faster per step.
             const int rel_claim = p.claim_ahead > 0 ? max(0, nrs - p.claim_ahead) : 0;
-            int batch_row = cur_row, next_batch = -1;
+            int batch_row = cur_row, next_blk = 0;
+            bool next_has = false;
             for (int rel = 0; rel < nrs; ++rel, ++it) {
                 const int st = cur.stage_begin + rel * G::kPSR;  // its first planner stage
                 if (rel % G::kRSB == 0) {
-                    if (rel > 0) batch_row = next_batch;
-                    next_batch = (rel + G::kRSB < nrs)
-                                     ? chunk_row_of(p, cur, cur_h, cur.seq_len, st + 8, lane)
-                                     : -1;
+                    // this batch's rows from the block ids loaded a batch ago;
+                    // then the next batch's ids, used only a batch from now
+                    if (rel > 0) batch_row = chunk_row_from(p, next_blk, next_has, cur_h, st, lane);
+                    next_has = false;
+                    if (rel + G::kRSB < nrs)
+                        next_blk = chunk_blk_load(p, cur, cur.seq_len, st + 8, lane, next_has);
                 }
                 if (rel == rel_claim && lane == 0)
                     nxt_idx = atomicAdd(&p.hdr->short_next, 1) + first_static;
@@ -543,8 +558,8 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                         pf = 1;
                     } else {
                         if (nxt_idx < num_items) {
-                            nxt_row = chunk_row_of(p, nxt, nxt_h, nxt.seq_len, nxt.stage_begin,
-                                                   lane);
+                            nxt_blk = chunk_blk_load(p, nxt, nxt.seq_len, nxt.stage_begin, lane,
+                                                     nxt_has);
                             nxt_q0 = __ldg(p.qsl + nxt.b);
                             nxt_ctx = __ldg(p.ctx + nxt.b);
                         }
@@ -559,7 +574,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                 const int slot = it % kStages;
                 int ok = 1;
                 if (lane == 0 && it >= kStages)
-                    ok = mbar_wait(&empty[slot], ((it / kStages) - 1) & 1, abort_flag);
+                    ok = mbar_wait_spin(&empty[slot], ((it / kStages) - 1) & 1, abort_flag);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 // test hook: stop after the first stage, as a producer would
                 // whose wait had run out
@@ -610,7 +625,9 @@ __global__ void __launch_bounds__(kShortThreads, 2)
             cur_idx = nxt_idx;
             cur = nxt;
             cur_h = nxt_h;
-            cur_row = nxt_row;
+            cur_row = cur_idx < num_items
+                          ? chunk_row_from(p, nxt_blk, nxt_has, nxt_h, nxt.stage_begin, lane)
+                          : -1;
             cur_q0 = nxt_q0;
             cur_ctx = nxt_ctx;
         }
@@ -630,7 +647,11 @@ __global__ void __launch_bounds__(kShortThreads, 2)
     uint32_t it = 0;
     while (true) {
         const int slot = it % kStages;
-        const bool ok = warp_mbar_wait(&full[slot], (it / kStages) & 1, abort_flag);
+        // bf16 consumers poll (they wait on data and leave issue slots to
+        // spare); the e4m3 consumers, bound by their own instruction issue,
+        // suspend instead (polling measured 1.9 % slower on that mixed step)
+        const bool ok = FP8 ? warp_mbar_wait(&full[slot], (it / kStages) & 1, abort_flag)
+                            : warp_mbar_wait_spin(&full[slot], (it / kStages) & 1, abort_flag);
         if (!ok) {
             if (lane == 0) flag_status(p.status, PA_DEV_WAIT_TIMEOUT);
             break;
