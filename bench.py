@@ -4,9 +4,10 @@
 Headline (`value`): query tokens/s of the mixed step -- 8 chunked-prefill
 chunks of 512 tokens (cached context uniform in 0..8192), 192 decode rows
 (seq_len uniform in 256..8192) and 32 speculative-verify rows of 1+4 tokens;
-32 q / 8 kv heads, head_dim 128, block_size 16, bf16.  One step = write the
-4448 new K/V rows through the slot mapping + attention for every row (device
-planner, split-KV kernel, tensor-core kernel, fused split merge).  Inputs are
+32 q / 8 kv heads, head_dim 128, block_size 16, bf16.  One step = one
+pa_write_kv_attention call: write the 4448 new K/V rows through the slot
+mapping + attention for every row (device planner, split-KV kernel,
+tensor-core kernel, fused split merge).  Inputs are
 resident in HBM and larger than L2 (about 3.9 GB of KV is read per step), so
 no L2 flush is needed between steps.
 
@@ -166,8 +167,16 @@ class DeviceStep:
                                            staging_blocks(step))
         self.ws = pk.alloc_workspace(nbytes, dev)
 
-    def run(self, write=True):
+    def run(self, write=True, fused=True):
+        """One step: the cache write and the attention, through the one-call
+        entry point (fused=True; the write runs beside the step's planner)
+        or as pa_write_kv then pa_attention; write=False attends only."""
         pk = self.pk
+        if write and fused:
+            pk.pa_write_kv_attention(self.k, self.v, self.slots, self.q, self.kc, self.vc,
+                                     self.bt, self.qsl, self.ctx, self.sl, self.step.scale,
+                                     self.out, self.lse, workspace=self.ws, **self.scales)
+            return
         if write:
             pk.pa_write_kv(self.k, self.v, self.slots, self.kc, self.vc, **self.scales)
         pk.pa_attention(self.q, self.kc, self.vc, self.bt, self.qsl, self.ctx, self.sl,
@@ -554,9 +563,9 @@ def run_ours(args):
                 b = i & 1
                 stream.wait_event(in_ready[b])
                 d, (o, l) = dbuf[b], outs[b]
-                pk.pa_write_kv(d["k"], d["v"], d["slots"], ds.kc, ds.vc, **ds.scales)
-                pk.pa_attention(d["q"], ds.kc, ds.vc, d["bt"], d["qsl"], d["ctx"], d["sl"],
-                                step.scale, o, l, workspace=ds.ws, **ds.scales)
+                pk.pa_write_kv_attention(d["k"], d["v"], d["slots"], d["q"], ds.kc, ds.vc,
+                                         d["bt"], d["qsl"], d["ctx"], d["sl"], step.scale, o,
+                                         l, workspace=ds.ws, **ds.scales)
                 done[b].record(stream)
                 with torch.cuda.stream(copy_stream):
                     if i + 1 < n:
@@ -676,7 +685,8 @@ def bench_graph_decode(args, dev):
     plan lets a serving loop remove."""
     from paged_kv_cache_284_gb300 import workloads
     res = {"workload": "decode rows, seq_len U[512,4096], 32 q / 8 kv heads, d=128, bs=16; "
-                       "write_kv + attention per step, back to back"}
+                       "one pa_write_kv_attention call (cache write + attention) per step, "
+                       "back to back"}
     for b in (8, 64):
         pool, (step,) = workloads.decode_heavy(seed=workloads.SEED_BASE + 50 + b, num_seqs=b)
         ds = DeviceStep(pool, step, dev)
@@ -734,7 +744,11 @@ def bench_fp8(args, dev, hbm_peak):
 
         def one(write=True):
             if write:
-                pk.pa_write_kv(k, v, slots, kc, vc, k_scale=ks, v_scale=vs)
+                pk.pa_write_kv_attention(k, v, slots, q, kc, vc, meta["block_tables"],
+                                         meta["query_start_loc"], meta["context_lens"],
+                                         meta["seq_lens"], step.scale, out, lse, workspace=ws,
+                                         k_scale=ks, v_scale=vs)
+                return
             pk.pa_attention(q, kc, vc, scale=step.scale, out=out, lse=lse, workspace=ws,
                             k_scale=ks, v_scale=vs, **meta)
 

@@ -174,6 +174,25 @@ int pa_attention(const void *q, const pa_kv_desc *kv, const int32_t *block_table
                  void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * One whole step in one call: pa_write_kv(k, v, slot_mapping,
+ * num_new_tokens, kv) followed by pa_attention(q, kv, ...) on the same
+ * stream, with the same arguments, rules, errors and results (caches bit for
+ * bit, out and lse), in one host call: the same kernels run in the same
+ * order, the write as a programmatic dependent of whatever ran before, so
+ * its launch overlaps that kernel's tail and it is off the step's critical
+ * path ([CH] §11.5: a decode step is dominated by fixed per-step costs;
+ * this call halves the host calls per step).  num_seqs == 0 or
+ * num_q_tokens == 0 does the write alone.
+ */
+int pa_write_kv_attention(const void *k, const void *v, const int64_t *slot_mapping,
+                          int32_t num_new_tokens, const void *q, const pa_kv_desc *kv,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *query_start_loc, const int32_t *context_lens,
+                          const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_tokens,
+                          int32_t num_q_heads, float scale, void *out, float *lse,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * pa_attention with the kernel choice exposed (tests, tuning):
  *   short_q_max_rows: a request whose q_len * group is at most this many
  *   rows runs on the split-KV kernel, the others on the tensor-core kernel.

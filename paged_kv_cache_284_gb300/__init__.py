@@ -32,6 +32,7 @@ PA_DEV_BAD_METADATA, PA_DEV_BAD_BLOCK, PA_DEV_BAD_SLOT, PA_DEV_WAIT_TIMEOUT, \
     PA_DEV_PLAN_OVERFLOW = 0x1, 0x2, 0x4, 0x8, 0x10
 
 EXPORTED = ["pa_write_kv", "pa_attention_workspace_size", "pa_attention", "pa_attention_ex",
+            "pa_write_kv_attention",
             "pa_merge_states", "pa_cascade_workspace_size", "pa_prefix_attention",
             "pa_cascade_decode", "pa_validate_metadata", "pa_last_error_message",
             "pa_status_string", "pa_read_device_status", "pa_set_profile_events",
@@ -79,6 +80,8 @@ def _declare(lib):
                          ctypes.c_int),
         "pa_attention_ex": ([P, KV, P, i32, P, P, P, i32, i32, i32, f32, P, P, P, sz, i32, i32,
                              P], ctypes.c_int),
+        "pa_write_kv_attention": ([P, P, P, i32, P, KV, P, i32, P, P, P, i32, i32, i32, f32, P, P,
+                                   P, sz, P], ctypes.c_int),
         "pa_merge_states": ([P, P, P, P, i32, i32, i32, P, P, P], ctypes.c_int),
         "pa_cascade_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
         "pa_prefix_attention": ([P, KV, P, i32, i32, i32, f32, P, P, P, sz, P], ctypes.c_int),
@@ -250,6 +253,41 @@ def pa_attention(q, k_cache, v_cache, block_tables, query_start_loc, context_len
                                  _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
                                  int(short_q_max_rows), int(split_keys), _stream(stream)),
            "pa_attention")
+    return workspace
+
+
+def pa_write_kv_attention(k, v, slot_mapping, q, k_cache, v_cache, block_tables,
+                          query_start_loc, context_lens, seq_lens, scale, out, lse=None,
+                          workspace=None, stream=None, k_scale=None, v_scale=None,
+                          staging_blocks=0):
+    """pa_write_kv then pa_attention in one call (same arguments, same
+    results); the cache write runs beside the step's planner.  Returns the
+    workspace tensor used."""
+    _need(k, "k", torch.bfloat16)
+    _need(v, "v", torch.bfloat16)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    _need(q, "q", torch.bfloat16)
+    _need(out, "out", torch.bfloat16)
+    for name, t in (("block_tables", block_tables), ("query_start_loc", query_start_loc),
+                    ("context_lens", context_lens), ("seq_lens", seq_lens)):
+        _need(t, name, torch.int32)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    kv = kv_desc(k_cache, v_cache, k_scale, v_scale)
+    T, hq, _ = q.shape
+    B = int(seq_lens.shape[0])
+    need = workspace_size(B, T, hq, kv.num_kv_heads, kv.head_dim)
+    if kv.kv_dtype == PA_KV_FP8_E4M3 and staging_blocks > 0:
+        need += fp8_staging_bytes(kv.num_kv_heads, kv.head_dim, kv.block_size, staging_blocks)
+    if workspace is None or workspace.numel() < need:
+        workspace = alloc_workspace(need, q.device)
+    _check(lib().pa_write_kv_attention(_ptr(k), _ptr(v), _ptr(slot_mapping), int(k.shape[0]),
+                                       _ptr(q), ctypes.byref(kv), _ptr(block_tables),
+                                       int(block_tables.shape[1]), _ptr(query_start_loc),
+                                       _ptr(context_lens), _ptr(seq_lens), B, T, hq,
+                                       float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                       workspace.numel(), _stream(stream)),
+           "pa_write_kv_attention")
     return workspace
 
 

@@ -357,15 +357,23 @@ struct CascadeArgs {
     float *suffix_o, *suffix_lse;  // suffix state per row, fp32
 };
 
+// The step's new K/V rows, for the call that writes them and attends.
+struct NewRows {
+    const void *k, *v;
+    const int64_t *slots;
+    int32_t num_tokens;
+};
+
 // Runs the planner, the split-KV kernel and the tensor-core kernel of one
 // step on `s`.  With `casc` (cascade decode, all rows short) the step is
 // the unique-suffix pass, run side by side with the shared-prefix pass.
+// With `fresh`, the step's new rows are written into the cache first.
 int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, int32_t max_blocks,
              const int32_t *qsl, const int32_t *ctx, const int32_t *seq_lens, int32_t num_seqs,
              int32_t T, int32_t Hq, float scale, void *out, float *lse, uint8_t *ws,
              const WsLayout &L, int short_max_rows, int split_keys, const CascadeArgs *casc,
              bool forbid_long, const StepMaps &maps, const Staging &stg, DeviceInfo *dev,
-             cudaStream_t s) {
+             cudaStream_t s, const NewRows *fresh = nullptr) {
     const int D = kv->head_dim;
     const int group = Hq / kv->num_kv_heads;
     const int tq = q_tile_tokens(group);
@@ -408,6 +416,17 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
     pp.num_counters = L.num_counters;
     pp.status = dev->status;
     int rc;
+    if (fresh && fresh->num_tokens > 0) {
+        // The step's new rows first, as pa_write_kv does: its kernel runs as a
+        // programmatic dependent ahead of the planner and is off the step's
+        // critical path.  (Writing them from copy blocks in the planner's
+        // grid measured no faster on an 8-request decode step and slower on
+        // large ones.)
+        ProfScope prof(PA_KERNEL_WRITE_KV, s);
+        rc = launch_write_kv(fresh->k, fresh->v, fresh->slots, fresh->num_tokens, kv, dev->status,
+                             s);
+        if (rc != PA_OK) return fail(rc, "write_kv launch failed");
+    }
     {
         ProfScope prof(PA_KERNEL_PLAN, s);
         rc = launch_plan(pp, s);
@@ -796,12 +815,27 @@ size_t pa_attention_workspace_size(int32_t num_seqs, int32_t num_q_tokens, int32
     return make_layout(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, 0, false).total;
 }
 
-int pa_attention_ex(const void *q, const pa_kv_desc *kv, const int32_t *block_tables,
+}  // extern "C"
+
+namespace {
+
+// Checks of pa_write_kv's arguments; num_tokens == 0 needs no pointers.
+int check_new_rows(const NewRows &nr) {
+    if (nr.num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
+    if (nr.num_tokens == 0) return PA_OK;
+    if (!nr.k || !nr.v || !nr.slots) return fail(PA_ERR_INVALID_ARG, "NULL input");
+    if (!aligned(nr.k, 16) || !aligned(nr.v, 16))
+        return fail(PA_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+    return PA_OK;
+}
+
+// pa_attention_ex, and with `fresh` the write of the step's new rows first.
+int attention_entry(const void *q, const pa_kv_desc *kv, const int32_t *block_tables,
                     int32_t max_blocks_per_seq, const int32_t *query_start_loc,
                     const int32_t *context_lens, const int32_t *seq_lens, int32_t num_seqs,
                     int32_t num_q_tokens, int32_t num_q_heads, float scale, void *out, float *lse,
                     void *workspace, size_t workspace_bytes, int32_t short_q_max_rows,
-                    int32_t split_keys, void *stream) {
+                    int32_t split_keys, cudaStream_t stream, const NewRows *fresh) {
     g_err[0] = 0;
     int rc = common_checks(q, kv, num_q_tokens, num_q_heads, scale, out, workspace);
     if (rc != PA_OK) return rc;
@@ -810,7 +844,17 @@ int pa_attention_ex(const void *q, const pa_kv_desc *kv, const int32_t *block_ta
         return fail(PA_ERR_INVALID_ARG, "short_q_max_rows must be -1 or in [0, %d]", kShortMaxRows);
     if (split_keys < 0 || split_keys % kStageKeys != 0)
         return fail(PA_ERR_INVALID_ARG, "split_keys must be 0 or a multiple of %d", kStageKeys);
-    if (num_seqs == 0 || num_q_tokens == 0) return PA_OK;
+    if (fresh && (rc = check_new_rows(*fresh)) != PA_OK) return rc;
+    if (num_seqs == 0 || num_q_tokens == 0) {
+        // nothing to attend: the write alone, as pa_write_kv
+        if (!fresh || fresh->num_tokens == 0) return PA_OK;
+        DeviceInfo *dev;
+        if ((rc = device_info(&dev)) != PA_OK) return rc;
+        ProfScope prof(PA_KERNEL_WRITE_KV, stream);
+        rc = launch_write_kv(fresh->k, fresh->v, fresh->slots, fresh->num_tokens, kv, dev->status,
+                             stream);
+        return rc == PA_OK ? PA_OK : fail(rc, "write_kv launch failed");
+    }
     if (!block_tables || !query_start_loc || !context_lens || !seq_lens)
         return fail(PA_ERR_INVALID_ARG, "metadata pointer is NULL");
     if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq <= 0");
@@ -832,8 +876,40 @@ int pa_attention_ex(const void *q, const pa_kv_desc *kv, const int32_t *block_ta
                     seq_lens, num_seqs, num_q_tokens, num_q_heads, scale, out, lse,
                     static_cast<uint8_t *>(workspace), L,
                     short_q_max_rows < 0 ? kShortMaxRows : short_q_max_rows, split_keys, nullptr,
-                    false, maps, stg, dev, static_cast<cudaStream_t>(stream));
+                    false, maps, stg, dev, stream, fresh);
 }
+
+}  // namespace
+
+extern "C" {
+
+int pa_attention_ex(const void *q, const pa_kv_desc *kv, const int32_t *block_tables,
+                    int32_t max_blocks_per_seq, const int32_t *query_start_loc,
+                    const int32_t *context_lens, const int32_t *seq_lens, int32_t num_seqs,
+                    int32_t num_q_tokens, int32_t num_q_heads, float scale, void *out, float *lse,
+                    void *workspace, size_t workspace_bytes, int32_t short_q_max_rows,
+                    int32_t split_keys, void *stream) {
+    return attention_entry(q, kv, block_tables, max_blocks_per_seq, query_start_loc,
+                               context_lens, seq_lens, num_seqs, num_q_tokens, num_q_heads, scale,
+                               out, lse, workspace, workspace_bytes, short_q_max_rows, split_keys,
+                               static_cast<cudaStream_t>(stream), nullptr);
+}
+
+int pa_write_kv_attention(const void *k, const void *v, const int64_t *slot_mapping,
+                          int32_t num_new_tokens, const void *q, const pa_kv_desc *kv,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *query_start_loc, const int32_t *context_lens,
+                          const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_tokens,
+                          int32_t num_q_heads, float scale, void *out, float *lse,
+                          void *workspace, size_t workspace_bytes, void *stream) {
+    const NewRows fresh{k, v, slot_mapping, num_new_tokens};
+    return attention_entry(q, kv, block_tables, max_blocks_per_seq, query_start_loc,
+                               context_lens, seq_lens, num_seqs, num_q_tokens, num_q_heads, scale,
+                               out, lse, workspace, workspace_bytes, -1, 0,
+                               static_cast<cudaStream_t>(stream), &fresh);
+}
+
+
 
 size_t pa_fp8_staging_bytes(int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                             int64_t num_blocks) {

@@ -3,48 +3,50 @@
 // fixed-size physical blocks; slot = block * block_size + offset).
 //
 // Pure HBM copy: each thread moves one 16-byte piece of one (token, kv head)
-// row for K and the same piece for V, so a warp covers 512 contiguous bytes
-// of the source and whole 16-byte sectors of the destination row.
+// row for K and the same piece for V, so a warp covers whole 16-byte sectors
+// of the destination rows.
 #include <cuda_fp8.h>
 
 #include "pa_internal.cuh"
 
 namespace pa {
 
-__global__ void __launch_bounds__(256) write_kv_kernel(
-    const uint4 *__restrict__ k, const uint4 *__restrict__ v, const int64_t *__restrict__ slots,
-    int num_tokens, int num_kv_heads, int pieces_per_row, int block_size, int num_blocks,
-    uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, unsigned *status) {
-    // k, v and the slots may come from the previous kernel, and that kernel
-    // may still read the cache
-    pdl_wait();
-    pdl_trigger();
-    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t per_token = static_cast<int64_t>(num_kv_heads) * pieces_per_row;
-    if (idx >= per_token * num_tokens) return;
+// The step's new K/V rows and their cache slots (reshape_and_cache).  A
+// piece is 16 bytes of one (token, kv head) cache row: 8 bf16 elements, or
+// 16 e4m3 codes quantised from 16 bf16 source elements.
+struct RowWrite {
+    const uint4 *k, *v;  // bf16 [num_tokens][num_kv_heads][head_dim]
+    const int64_t *slots;
+    uint4 *k_cache, *v_cache;
+    const float *k_scale, *v_scale;  // fp8 pool only
+    int num_tokens, num_kv_heads, pieces_per_row, block_size, num_blocks, fp8;
+    __host__ __device__ int64_t pieces() const {
+        return static_cast<int64_t>(num_tokens) * num_kv_heads * pieces_per_row;
+    }
+};
+
+// Cache piece of RowWrite piece idx (< w.pieces()), or -1 for a padding
+// token (negative slot) or a slot beyond the pool (flagged).
+__device__ __forceinline__ int64_t row_piece_dst(const RowWrite &w, int64_t idx,
+                                                 unsigned *status) {
+    const int64_t per_token = static_cast<int64_t>(w.num_kv_heads) * w.pieces_per_row;
     const int64_t t = idx / per_token;
     const int64_t rem = idx - t * per_token;  // = h * pieces_per_row + piece
-    const int64_t s = __ldg(slots + t);
-    if (s < 0) return;  // padding token
-    const int64_t blk = s / block_size;
-    const int64_t off = s - blk * block_size;
-    if (blk >= num_blocks) {
+    const int64_t s = __ldg(w.slots + t);
+    if (s < 0) return -1;
+    const int64_t blk = s / w.block_size;
+    const int64_t off = s - blk * w.block_size;
+    if (blk >= w.num_blocks) {
         flag_status(status, PA_DEV_BAD_SLOT);
-        return;
+        return -1;
     }
-    const int64_t h = rem / pieces_per_row;
-    const int64_t piece = rem - h * pieces_per_row;
-    const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * pieces_per_row + piece;
-    const uint4 kv_k = __ldg(k + idx);
-    const uint4 kv_v = __ldg(v + idx);
-    k_cache[dst] = kv_k;
-    v_cache[dst] = kv_v;
+    const int64_t h = rem / w.pieces_per_row;
+    const int64_t piece = rem - h * w.pieces_per_row;
+    return ((blk * w.num_kv_heads + h) * w.block_size + off) * w.pieces_per_row + piece;
 }
 
-// FP8 pool: each thread turns 16 bf16 elements of one (token, kv head) row
-// into 16 e4m3 codes, x / scale[h] in binary32 (IEEE division) then the
-// saturating round-to-nearest-even conversion, and stores them as one
-// 16-byte piece of the cache row.
+// Four bf16 elements to four e4m3 codes: x / scale in binary32 (IEEE
+// division), then the saturating round-to-nearest-even conversion.
 __device__ __forceinline__ uint32_t quantise4(uint2 x, float s) {
     const float f0 = __fdiv_rn(__uint_as_float(x.x << 16), s);
     const float f1 = __fdiv_rn(__uint_as_float(x.x & 0xFFFF0000u), s);
@@ -54,65 +56,79 @@ __device__ __forceinline__ uint32_t quantise4(uint2 x, float s) {
     const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f2, f3), __NV_SATFINITE, __NV_E4M3);
     return (lo & 0xFFFFu) | (hi << 16);
 }
+__device__ __forceinline__ uint4 quantise16(uint4 a, uint4 b, float s) {
+    return make_uint4(quantise4(make_uint2(a.x, a.y), s), quantise4(make_uint2(a.z, a.w), s),
+                      quantise4(make_uint2(b.x, b.y), s), quantise4(make_uint2(b.z, b.w), s));
+}
 
-__global__ void __launch_bounds__(256) write_kv_fp8_kernel(
-    const uint4 *__restrict__ k, const uint4 *__restrict__ v, const int64_t *__restrict__ slots,
-    int num_tokens, int num_kv_heads, int pieces_per_row, int block_size, int num_blocks,
-    const float *__restrict__ k_scale, const float *__restrict__ v_scale,
-    uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, unsigned *status) {
+// Writes K and V piece idx (< w.pieces()) of the new rows into a bf16
+// pool's cache: a bit copy.
+__device__ __forceinline__ void write_row_piece_bf16(const RowWrite &w, int64_t idx,
+                                                     unsigned *status) {
+    const int64_t dst = row_piece_dst(w, idx, status);
+    if (dst < 0) return;
+    const uint4 k = __ldg(w.k + idx), v = __ldg(w.v + idx);
+    w.k_cache[dst] = k;
+    w.v_cache[dst] = v;
+}
+
+// The same on an fp8 pool: the 16 bf16 source elements of the piece
+// quantised with kv head h's scale.
+__device__ __forceinline__ void write_row_piece_fp8(const RowWrite &w, int64_t idx,
+                                                    unsigned *status) {
+    const int64_t dst = row_piece_dst(w, idx, status);
+    if (dst < 0) return;
+    const int h = static_cast<int>((idx / w.pieces_per_row) % w.num_kv_heads);
+    const float ks = __ldg(w.k_scale + h), vs = __ldg(w.v_scale + h);
+    const uint4 ka = __ldg(w.k + 2 * idx), kb = __ldg(w.k + 2 * idx + 1);
+    const uint4 va = __ldg(w.v + 2 * idx), vb = __ldg(w.v + 2 * idx + 1);
+    w.k_cache[dst] = quantise16(ka, kb, ks);
+    w.v_cache[dst] = quantise16(va, vb, vs);
+}
+
+static RowWrite make_row_write(const void *k, const void *v, const int64_t *slots,
+                               int num_tokens, const pa_kv_desc *kv) {
+    RowWrite w{};
+    w.k = static_cast<const uint4 *>(k);
+    w.v = static_cast<const uint4 *>(v);
+    w.slots = slots;
+    w.k_cache = static_cast<uint4 *>(kv->k_cache);
+    w.v_cache = static_cast<uint4 *>(kv->v_cache);
+    w.fp8 = kv->kv_dtype == PA_KV_FP8_E4M3 ? 1 : 0;
+    w.k_scale = w.fp8 ? kv->k_scale : nullptr;
+    w.v_scale = w.fp8 ? kv->v_scale : nullptr;
+    w.num_tokens = num_tokens;
+    w.num_kv_heads = kv->num_kv_heads;
+    // a 16-byte cache piece holds 8 bf16 elements or 16 e4m3 codes
+    w.pieces_per_row = w.fp8 ? kv->head_dim / 16 : kv->head_dim / 8;
+    w.block_size = kv->block_size;
+    w.num_blocks = kv->num_blocks;
+    return w;
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(256) write_kv_kernel(const RowWrite w, unsigned *status) {
+    // k, v and the slots may come from the previous kernel, and that kernel
+    // may still read the cache
     pdl_wait();
     pdl_trigger();
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t per_token = static_cast<int64_t>(num_kv_heads) * pieces_per_row;
-    if (idx >= per_token * num_tokens) return;
-    const int64_t t = idx / per_token;
-    const int64_t rem = idx - t * per_token;  // = h * pieces_per_row + piece
-    const int64_t s = __ldg(slots + t);
-    if (s < 0) return;  // padding token
-    const int64_t blk = s / block_size;
-    const int64_t off = s - blk * block_size;
-    if (blk >= num_blocks) {
-        flag_status(status, PA_DEV_BAD_SLOT);
-        return;
-    }
-    const int64_t h = rem / pieces_per_row;
-    const int64_t piece = rem - h * pieces_per_row;
-    const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * pieces_per_row + piece;
-    const float ks = __ldg(k_scale + h), vs = __ldg(v_scale + h);
-    // source: 16 bf16 = two 16-byte pieces of the bf16 row
-    const uint4 ka = __ldg(k + 2 * idx), kb = __ldg(k + 2 * idx + 1);
-    const uint4 va = __ldg(v + 2 * idx), vb = __ldg(v + 2 * idx + 1);
-    k_cache[dst] = make_uint4(quantise4(make_uint2(ka.x, ka.y), ks), quantise4(make_uint2(ka.z, ka.w), ks),
-                              quantise4(make_uint2(kb.x, kb.y), ks), quantise4(make_uint2(kb.z, kb.w), ks));
-    v_cache[dst] = make_uint4(quantise4(make_uint2(va.x, va.y), vs), quantise4(make_uint2(va.z, va.w), vs),
-                              quantise4(make_uint2(vb.x, vb.y), vs), quantise4(make_uint2(vb.z, vb.w), vs));
+    if (idx >= w.pieces()) return;
+    if (FP8)
+        write_row_piece_fp8(w, idx, status);
+    else
+        write_row_piece_bf16(w, idx, status);
 }
 
 int launch_write_kv(const void *k, const void *v, const int64_t *slots, int num_tokens,
                     const pa_kv_desc *kv, unsigned *status, cudaStream_t s) {
     if (num_tokens == 0) return PA_OK;
-    if (kv->kv_dtype == PA_KV_FP8_E4M3) {
-        const int pieces = kv->head_dim / 16;  // 16 codes per 16-byte piece
-        const int64_t total = static_cast<int64_t>(num_tokens) * kv->num_kv_heads * pieces;
-        const int threads = 256;
-        const int64_t blocks = (total + threads - 1) / threads;
-        PdlLaunch l(static_cast<unsigned>(blocks), threads, 0, s);
-        const cudaError_t e = launch_kernel(
-            l, write_kv_fp8_kernel, static_cast<const uint4 *>(k),
-            static_cast<const uint4 *>(v), slots, num_tokens, kv->num_kv_heads, pieces,
-            kv->block_size, kv->num_blocks, kv->k_scale, kv->v_scale,
-            static_cast<uint4 *>(kv->k_cache), static_cast<uint4 *>(kv->v_cache), status);
-        return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
-    }
-    const int pieces = kv->head_dim * 2 / 16;
-    const int64_t total = static_cast<int64_t>(num_tokens) * kv->num_kv_heads * pieces;
+    const RowWrite w = make_row_write(k, v, slots, num_tokens, kv);
     const int threads = 256;
-    const int64_t blocks = (total + threads - 1) / threads;
+    const int64_t blocks = (w.pieces() + threads - 1) / threads;
     PdlLaunch l(static_cast<unsigned>(blocks), threads, 0, s);
-    const cudaError_t e = launch_kernel(
-        l, write_kv_kernel, static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slots,
-        num_tokens, kv->num_kv_heads, pieces, kv->block_size, kv->num_blocks,
-        static_cast<uint4 *>(kv->k_cache), static_cast<uint4 *>(kv->v_cache), status);
+    const cudaError_t e = w.fp8 ? launch_kernel(l, write_kv_kernel<true>, w, status)
+                                : launch_kernel(l, write_kv_kernel<false>, w, status);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
