@@ -181,8 +181,10 @@ __device__ __forceinline__ ShortItem short_work(const ShortParams &p, int idx, i
 // Lane (g = lane/4, t = lane%4) holds scores of keys g, g+8 for rows 2t,
 // 2t+1, and O^T tile cc's elements (dim 16cc+2g | 16cc+2g+1) x (row 2t |
 // 2t+1): cs.o[cc][0] = (row 2t, dim 16cc+2g), [1] = (2t+1, 16cc+2g),
-// [2] = (2t, 16cc+2g+1), [3] = (2t+1, 16cc+2g+1).
-template <int D, int NC>
+// [2] = (2t, 16cc+2g+1), [3] = (2t+1, 16cc+2g+1).  CHECK = false: every
+// key of the chunks is below the item's end and visible to every row (the
+// caller checked), so the masks and the V-tail zeroing are compiled out.
+template <int D, int NC, bool CHECK>
 __device__ __forceinline__ void swapped_chunks(Consumer<D> &cs, const uint32_t (&kb)[NC],
                                                const uint32_t (&vb)[NC], const int (&key0)[NC],
                                                int lane) {
@@ -220,7 +222,7 @@ __device__ __forceinline__ void swapped_chunks(Consumer<D> &cs, const uint32_t (
 #pragma unroll
     for (int n = 0; n < NC; ++n) {
         const bool need_mask =
-            (key0[n] + kChunkKeys - 1 > cs.ctx) || (key0[n] + kChunkKeys > cs.key_end);
+            CHECK && ((key0[n] + kChunkKeys - 1 > cs.ctx) || (key0[n] + kChunkKeys > cs.key_end));
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             s[n][e] = (st[n][0][e] + st[n][1][e]) * cs.sl2;
@@ -281,7 +283,7 @@ __device__ __forceinline__ void swapped_chunks(Consumer<D> &cs, const uint32_t (
 #pragma unroll
     for (int n = 0; n < NC; ++n) {
         const int nvalid = cs.key_end - key0[n];
-        tail[n] = nvalid < kChunkKeys;
+        tail[n] = CHECK && nvalid < kChunkKeys;
         k0[n] = 2 * t < nvalid;
         k1[n] = 2 * t + 1 < nvalid;
         k8[n] = 2 * t + 8 < nvalid;
@@ -772,12 +774,20 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                         const uint32_t vbs[2] = {smem_u32(v_box(slot, cs.kq, 0)),
                                                  smem_u32(v_box(slot, cs.kq + cs.KQ, 0))};
                         const int ks0[2] = {ka, kb2};
-                        swapped_chunks<D, 2>(cs, kbs, vbs, ks0, lane);
+                        // the later chunk's last key decides: below the
+                        // item's end and the first row's causal limit, no
+                        // key of either chunk needs a mask (one uniform
+                        // branch instead of ten per stage)
+                        const int last = kb2 + kChunkKeys - 1;
+                        if (last < cs.key_end && last <= cs.ctx)
+                            swapped_chunks<D, 2, false>(cs, kbs, vbs, ks0, lane);
+                        else
+                            swapped_chunks<D, 2, true>(cs, kbs, vbs, ks0, lane);
                     } else {
                         const uint32_t kbs[1] = {smem_u32(k_box(slot, cs.kq, 0))};
                         const uint32_t vbs[1] = {smem_u32(v_box(slot, cs.kq, 0))};
                         const int ks0[1] = {ka};
-                        swapped_chunks<D, 1>(cs, kbs, vbs, ks0, lane);
+                        swapped_chunks<D, 1, true>(cs, kbs, vbs, ks0, lane);
                     }
                 }
             }
