@@ -41,6 +41,8 @@
 //    the second MMA's B operand through movmatrix (8x8 transposes).  The
 //    row maximum is reduced across lanes only when some score exceeds the
 //    running maximum by more than 2^8 (the lazy rescale threshold).
+#include <type_traits>
+
 #include "pa_internal.cuh"
 
 namespace pa {
@@ -799,148 +801,159 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                 const uint32_t kb = smem_u32(k_box(slot, c, 0));
                 const uint32_t vb = smem_u32(v_box(slot, c, 0));
                 const int mi = lane >> 3;
-                float sacc[2][4];
+                // The chunk in two compiled forms: CHECK = false when all its
+                // keys are below the item's end and visible to every row, so
+                // the masks and the V-tail zeroing are compiled out (one
+                // uniform branch instead of one per mask and V load group).
+                auto chunk = [&](auto check_tag) {
+                    constexpr bool CHECK = decltype(check_tag)::value;
+                    float sacc[2][4];
 #pragma unroll
-                for (int i = 0; i < 2; ++i)
+                    for (int i = 0; i < 2; ++i)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) sacc[i][e] = 0.f;
-                if constexpr (FP8) {
+                        for (int e = 0; e < 4; ++e) sacc[i][e] = 0.f;
+                    if constexpr (FP8) {
 #pragma unroll
-                    for (int ks2 = 0; ks2 < KS / 2; ++ks2) {
-                        // matrices: keys 0-7 | 8-15 of k-step 2ks2, then of 2ks2+1
-                        const int key = (mi & 1) * 8 + (lane & 7);
-                        const int col = ks2 * 2 + (mi >> 1);
-                        uint32_t r[4];
-                        ldsm_x4(kb + sw128_offset(key, col), r[0], r[1], r[2], r[3]);
+                        for (int ks2 = 0; ks2 < KS / 2; ++ks2) {
+                            // matrices: keys 0-7 | 8-15 of k-step 2ks2, then of 2ks2+1
+                            const int key = (mi & 1) * 8 + (lane & 7);
+                            const int col = ks2 * 2 + (mi >> 1);
+                            uint32_t r[4];
+                            ldsm_x4(kb + sw128_offset(key, col), r[0], r[1], r[2], r[3]);
 #pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const int ks = ks2 * 2 + (m >> 1);
-                            uint32_t b0, b1;
-                            e4m3x4_to_f16x2x2(r[m], b0, b1);
-                            mma_f16_16816(sacc[m & 1], cs.qa[ks][0], cs.qa[ks][1], cs.qa[ks][2],
-                                          cs.qa[ks][3], b0, b1);
+                            for (int m = 0; m < 4; ++m) {
+                                const int ks = ks2 * 2 + (m >> 1);
+                                uint32_t b0, b1;
+                                e4m3x4_to_f16x2x2(r[m], b0, b1);
+                                mma_f16_16816(sacc[m & 1], cs.qa[ks][0], cs.qa[ks][1], cs.qa[ks][2],
+                                              cs.qa[ks][3], b0, b1);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int ks = 0; ks < KS; ++ks) {
+                            const int key = (mi >> 1) * 8 + (lane & 7);
+                            const int col = (ks & 3) * 2 + (mi & 1);
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4(kb + (ks >> 2) * G::kBoxBytes + sw128_offset(key, col), b0, b1,
+                                    b2, b3);
+                            mma_bf16_16816(sacc[0], cs.qa[ks][0], cs.qa[ks][1], cs.qa[ks][2],
+                                           cs.qa[ks][3], b0, b1);
+                            mma_bf16_16816(sacc[1], cs.qa[ks][0], cs.qa[ks][1], cs.qa[ks][2],
+                                           cs.qa[ks][3], b2, b3);
                         }
                     }
-                } else {
+                    // scale to log2 units and mask (causal limit per row, item key range)
+                    const bool need_mask = CHECK && ((key0 + kChunkKeys - 1 > cs.ctx) ||
+                                                     (key0 + kChunkKeys > cs.key_end));
 #pragma unroll
-                    for (int ks = 0; ks < KS; ++ks) {
-                        const int key = (mi >> 1) * 8 + (lane & 7);
-                        const int col = (ks & 3) * 2 + (mi & 1);
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(kb + (ks >> 2) * G::kBoxBytes + sw128_offset(key, col), b0, b1,
-                                b2, b3);
-                        mma_bf16_16816(sacc[0], cs.qa[ks][0], cs.qa[ks][1], cs.qa[ks][2],
-                                       cs.qa[ks][3], b0, b1);
-                        mma_bf16_16816(sacc[1], cs.qa[ks][0], cs.qa[ks][1], cs.qa[ks][2],
-                                       cs.qa[ks][3], b2, b3);
-                    }
-                }
-                // scale to log2 units and mask (causal limit per row, item key range)
-                const bool need_mask = (key0 + kChunkKeys - 1 > cs.ctx) ||
-                                       (key0 + kChunkKeys > cs.key_end);
+                    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float s = sacc[nt][e] * cs.sl2;
-                        if (need_mask) {
-                            const int key = key0 + nt * 8 + 2 * t + (e & 1);
-                            const int lim = (e < 2) ? cs.limit0 : cs.limit1;
-                            if (key > lim || key >= cs.key_end) s = -INFINITY;
+                        for (int e = 0; e < 4; ++e) {
+                            float s = sacc[nt][e] * cs.sl2;
+                            if (need_mask) {
+                                const int key = key0 + nt * 8 + 2 * t + (e & 1);
+                                const int lim = (e < 2) ? cs.limit0 : cs.limit1;
+                                if (key > lim || key >= cs.key_end) s = -INFINITY;
+                            }
+                            sacc[nt][e] = s;
                         }
-                        sacc[nt][e] = s;
-                    }
-                float mx0 = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
-                float mx1 = fmaxf(fmaxf(sacc[0][2], sacc[0][3]), fmaxf(sacc[1][2], sacc[1][3]));
-                mx0 = quad_max(mx0);
-                mx1 = quad_max(mx1);
-                const bool up0 = mx0 > cs.m0 + kRescaleThreshold || (cs.m0 == -INFINITY && mx0 > -INFINITY);
-                const bool up1 = mx1 > cs.m1 + kRescaleThreshold || (cs.m1 == -INFINITY && mx1 > -INFINITY);
-                if (__any_sync(0xffffffffu, up0 || up1)) {
-                    const float nm0 = up0 ? mx0 : cs.m0;
-                    const float nm1 = up1 ? mx1 : cs.m1;
-                    const float a0 = up0 ? (cs.m0 == -INFINITY ? 0.f : exp2f(cs.m0 - nm0)) : 1.f;
-                    const float a1 = up1 ? (cs.m1 == -INFINITY ? 0.f : exp2f(cs.m1 - nm1)) : 1.f;
-                    cs.m0 = nm0;
-                    cs.m1 = nm1;
-                    cs.l0 *= a0;
-                    cs.l1 *= a1;
+                    float mx0 = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
+                    float mx1 = fmaxf(fmaxf(sacc[0][2], sacc[0][3]), fmaxf(sacc[1][2], sacc[1][3]));
+                    mx0 = quad_max(mx0);
+                    mx1 = quad_max(mx1);
+                    const bool up0 = mx0 > cs.m0 + kRescaleThreshold || (cs.m0 == -INFINITY && mx0 > -INFINITY);
+                    const bool up1 = mx1 > cs.m1 + kRescaleThreshold || (cs.m1 == -INFINITY && mx1 > -INFINITY);
+                    if (__any_sync(0xffffffffu, up0 || up1)) {
+                        const float nm0 = up0 ? mx0 : cs.m0;
+                        const float nm1 = up1 ? mx1 : cs.m1;
+                        const float a0 = up0 ? (cs.m0 == -INFINITY ? 0.f : exp2f(cs.m0 - nm0)) : 1.f;
+                        const float a1 = up1 ? (cs.m1 == -INFINITY ? 0.f : exp2f(cs.m1 - nm1)) : 1.f;
+                        cs.m0 = nm0;
+                        cs.m1 = nm1;
+                        cs.l0 *= a0;
+                        cs.l1 *= a1;
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        cs.o[nt][0] *= a0;
-                        cs.o[nt][1] *= a0;
-                        cs.o[nt][2] *= a1;
-                        cs.o[nt][3] *= a1;
-                    }
-                }
-                const float ref0 = cs.m0 == -INFINITY ? 0.f : cs.m0;
-                const float ref1 = cs.m1 == -INFINITY ? 0.f : cs.m1;
-                float pr[2][4];
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    pr[nt][0] = exp2f(sacc[nt][0] - ref0);
-                    pr[nt][1] = exp2f(sacc[nt][1] - ref0);
-                    pr[nt][2] = exp2f(sacc[nt][2] - ref1);
-                    pr[nt][3] = exp2f(sacc[nt][3] - ref1);
-                }
-                cs.l0 += pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
-                cs.l1 += pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
-                const uint32_t pa0 = FP8 ? pack_f16x2(pr[0][0], pr[0][1]) : pack_bf16x2(pr[0][0], pr[0][1]);
-                const uint32_t pa1 = FP8 ? pack_f16x2(pr[0][2], pr[0][3]) : pack_bf16x2(pr[0][2], pr[0][3]);
-                const uint32_t pa2 = FP8 ? pack_f16x2(pr[1][0], pr[1][1]) : pack_bf16x2(pr[1][0], pr[1][1]);
-                const uint32_t pa3 = FP8 ? pack_f16x2(pr[1][2], pr[1][3]) : pack_bf16x2(pr[1][2], pr[1][3]);
-                // V rows past the item's keys may hold anything (even NaN):
-                // zero them in the fragments of a partially valid chunk.
-                const int nvalid = cs.key_end - key0;
-                const bool tail = nvalid < kChunkKeys;
-                const bool k0 = 2 * t < nvalid, k1 = 2 * t + 1 < nvalid;
-                const bool k8 = 2 * t + 8 < nvalid, k9 = 2 * t + 9 < nvalid;
-                if constexpr (FP8) {
-#pragma unroll
-                    for (int c2 = 0; c2 < D / 32; ++c2) {
-                        // matrices: keys 0-7 | 8-15 of dim group 2c2, then of 2c2+1;
-                        // lane: keys 2t, 2t+1 x dims 2j, 2j+1 (j = lane / 4)
-                        const int key = (mi & 1) * 8 + (lane & 7);
-                        const int col = c2 * 2 + (mi >> 1);
-                        uint32_t r[4];
-                        ldsm_x4_t(vb + sw128_offset(key, col), r[0], r[1], r[2], r[3]);
-                        if (tail) {
-                            r[0] = keep_pair(r[0], k0, k1);
-                            r[2] = keep_pair(r[2], k0, k1);
-                            r[1] = keep_pair(r[1], k8, k9);
-                            r[3] = keep_pair(r[3], k8, k9);
-                        }
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) r[m] = byte_perm(r[m], 0x3120u);
-                        // low halves: dim 2j (even tile), high halves: dim 2j+1 (odd tile)
-#pragma unroll
-                        for (int gsub = 0; gsub < 2; ++gsub) {
-                            // keys 0-7 (b0) and 8-15 (b1) of the even and odd tile
-                            uint32_t e0, o0, e1, o1;
-                            e4m3x4_to_f16x2x2(r[2 * gsub], e0, o0);
-                            e4m3x4_to_f16x2x2(r[2 * gsub + 1], e1, o1);
-                            mma_f16_16816(cs.o[4 * c2 + 2 * gsub], pa0, pa1, pa2, pa3, e0, e1);
-                            mma_f16_16816(cs.o[4 * c2 + 2 * gsub + 1], pa0, pa1, pa2, pa3, o0, o1);
+                        for (int nt = 0; nt < NT; ++nt) {
+                            cs.o[nt][0] *= a0;
+                            cs.o[nt][1] *= a0;
+                            cs.o[nt][2] *= a1;
+                            cs.o[nt][3] *= a1;
                         }
                     }
-                } else {
+                    const float ref0 = cs.m0 == -INFINITY ? 0.f : cs.m0;
+                    const float ref1 = cs.m1 == -INFINITY ? 0.f : cs.m1;
+                    float pr[2][4];
 #pragma unroll
-                    for (int dp = 0; dp < KS; ++dp) {
-                        const int key = (mi & 1) * 8 + (lane & 7);
-                        const int col = (dp & 3) * 2 + (mi >> 1);
-                        uint32_t v0, v1, v2, v3;
-                        ldsm_x4_t(vb + (dp >> 2) * G::kBoxBytes + sw128_offset(key, col), v0, v1,
-                                  v2, v3);
-                        if (tail) {
-                            v0 = keep_pair(v0, k0, k1);
-                            v2 = keep_pair(v2, k0, k1);
-                            v1 = keep_pair(v1, k8, k9);
-                            v3 = keep_pair(v3, k8, k9);
-                        }
-                        mma_bf16_16816(cs.o[2 * dp], pa0, pa1, pa2, pa3, v0, v1);
-                        mma_bf16_16816(cs.o[2 * dp + 1], pa0, pa1, pa2, pa3, v2, v3);
+                    for (int nt = 0; nt < 2; ++nt) {
+                        pr[nt][0] = exp2f(sacc[nt][0] - ref0);
+                        pr[nt][1] = exp2f(sacc[nt][1] - ref0);
+                        pr[nt][2] = exp2f(sacc[nt][2] - ref1);
+                        pr[nt][3] = exp2f(sacc[nt][3] - ref1);
                     }
-                }
+                    cs.l0 += pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
+                    cs.l1 += pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
+                    const uint32_t pa0 = FP8 ? pack_f16x2(pr[0][0], pr[0][1]) : pack_bf16x2(pr[0][0], pr[0][1]);
+                    const uint32_t pa1 = FP8 ? pack_f16x2(pr[0][2], pr[0][3]) : pack_bf16x2(pr[0][2], pr[0][3]);
+                    const uint32_t pa2 = FP8 ? pack_f16x2(pr[1][0], pr[1][1]) : pack_bf16x2(pr[1][0], pr[1][1]);
+                    const uint32_t pa3 = FP8 ? pack_f16x2(pr[1][2], pr[1][3]) : pack_bf16x2(pr[1][2], pr[1][3]);
+                    // V rows past the item's keys may hold anything (even NaN):
+                    // zero them in the fragments of a partially valid chunk.
+                    const int nvalid = cs.key_end - key0;
+                    const bool tail = CHECK && nvalid < kChunkKeys;
+                    const bool k0 = 2 * t < nvalid, k1 = 2 * t + 1 < nvalid;
+                    const bool k8 = 2 * t + 8 < nvalid, k9 = 2 * t + 9 < nvalid;
+                    if constexpr (FP8) {
+#pragma unroll
+                        for (int c2 = 0; c2 < D / 32; ++c2) {
+                            // matrices: keys 0-7 | 8-15 of dim group 2c2, then of 2c2+1;
+                            // lane: keys 2t, 2t+1 x dims 2j, 2j+1 (j = lane / 4)
+                            const int key = (mi & 1) * 8 + (lane & 7);
+                            const int col = c2 * 2 + (mi >> 1);
+                            uint32_t r[4];
+                            ldsm_x4_t(vb + sw128_offset(key, col), r[0], r[1], r[2], r[3]);
+                            if (tail) {
+                                r[0] = keep_pair(r[0], k0, k1);
+                                r[2] = keep_pair(r[2], k0, k1);
+                                r[1] = keep_pair(r[1], k8, k9);
+                                r[3] = keep_pair(r[3], k8, k9);
+                            }
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) r[m] = byte_perm(r[m], 0x3120u);
+                            // low halves: dim 2j (even tile), high halves: dim 2j+1 (odd tile)
+#pragma unroll
+                            for (int gsub = 0; gsub < 2; ++gsub) {
+                                // keys 0-7 (b0) and 8-15 (b1) of the even and odd tile
+                                uint32_t e0, o0, e1, o1;
+                                e4m3x4_to_f16x2x2(r[2 * gsub], e0, o0);
+                                e4m3x4_to_f16x2x2(r[2 * gsub + 1], e1, o1);
+                                mma_f16_16816(cs.o[4 * c2 + 2 * gsub], pa0, pa1, pa2, pa3, e0, e1);
+                                mma_f16_16816(cs.o[4 * c2 + 2 * gsub + 1], pa0, pa1, pa2, pa3, o0, o1);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int dp = 0; dp < KS; ++dp) {
+                            const int key = (mi & 1) * 8 + (lane & 7);
+                            const int col = (dp & 3) * 2 + (mi >> 1);
+                            uint32_t v0, v1, v2, v3;
+                            ldsm_x4_t(vb + (dp >> 2) * G::kBoxBytes + sw128_offset(key, col), v0, v1,
+                                      v2, v3);
+                            if (tail) {
+                                v0 = keep_pair(v0, k0, k1);
+                                v2 = keep_pair(v2, k0, k1);
+                                v1 = keep_pair(v1, k8, k9);
+                                v3 = keep_pair(v3, k8, k9);
+                            }
+                            mma_bf16_16816(cs.o[2 * dp], pa0, pa1, pa2, pa3, v0, v1);
+                            mma_bf16_16816(cs.o[2 * dp + 1], pa0, pa1, pa2, pa3, v2, v3);
+                        }
+                    }
+                };
+                if (key0 + kChunkKeys - 1 > cs.ctx || key0 + kChunkKeys > cs.key_end)
+                    chunk(std::true_type{});
+                else
+                    chunk(std::false_type{});
             }
         }
 
@@ -961,7 +974,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                     wrote_stage = true;
                     if (cs.active && cs.kq > 0) {
                         float *reg = scratch + (cs.rt * (cs.KQ - 1) + cs.kq - 1) * G::kScratchFloats;
-    #pragma unroll
+#pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             *reinterpret_cast<float2 *>(reg + g * D + nt * 8 + 2 * t) =
                                 make_float2(cs.o[nt][0], cs.o[nt][1]);
@@ -990,7 +1003,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                             l1 = a1 * l1 + b1 * ol1;
                             cs.m0 = M0;
                             cs.m1 = M1;
-    #pragma unroll
+#pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
                                 const float2 x = *reinterpret_cast<const float2 *>(reg + g * D + nt * 8 + 2 * t);
                                 const float2 y = *reinterpret_cast<const float2 *>(reg + (g + 8) * D + nt * 8 + 2 * t);
@@ -1019,7 +1032,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                             return pi * 8 + 2 * t;
                         }
                     };
-    #pragma unroll
+#pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const int r = cs.rt * 16 + g + half * 8;
                         if (r >= cs.R) continue;
@@ -1033,7 +1046,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                         if (cs.nsplit == 1) {
                             if (p.out_f32) {
                                 float *dst = p.out_f32 + row * D;
-    #pragma unroll
+#pragma unroll
                                 for (int pi = 0; pi < NT; ++pi) {
                                     float x, y;
                                     const int col = pair_of(pi, half, x, y);
@@ -1042,7 +1055,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                                 }
                             } else {
                                 uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + row * D);
-    #pragma unroll
+#pragma unroll
                                 for (int pi = 0; pi < NT; ++pi) {
                                     float x, y;
                                     const int col = pair_of(pi, half, x, y);
@@ -1052,7 +1065,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                             if (p.lse && t == 0) p.lse[row] = lse_v;
                         } else {
                             float *dst = p.partial_o + static_cast<int64_t>(cs.partial_base + r) * D;
-    #pragma unroll
+#pragma unroll
                             for (int pi = 0; pi < NT; ++pi) {
                                 float x, y;
                                 const int col = pair_of(pi, half, x, y);
