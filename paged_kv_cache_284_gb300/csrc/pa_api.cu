@@ -597,10 +597,12 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
         l1.wait_start = 1;
         l1.first_done = &hdr->first_done;
         l1.first_ctas = -1;
-        // share of the SMs measured best on the mixed step: a third beside the
-        // HBM-bound bf16 split-KV kernel; a tenth beside the fp8 one, whose
-        // rate follows its SM count
-        const int g1 = std::min(std::max(1, fp8 ? dev->sms / 10 : dev->sms / 3), long_grid);
+        // share of the SMs measured best on the mixed step: two fifths beside
+        // the HBM-bound bf16 split-KV kernel (60 of 152 SMs: 767.9 us per step,
+        // against 769.6 with 56, 773.4 with 64 and 785.4 with 50); a tenth
+        // beside the fp8 one, whose rate follows its SM count (707.3 us, 710.1
+        // with an eighth)
+        const int g1 = std::min(std::max(1, fp8 ? dev->sms / 10 : dev->sms * 2 / 5), long_grid);
         rc = launch_long(l1, maps.q, lk, lv, D, g1, s);
         if (rc != PA_OK) return fail(rc, "tensor-core kernel launch failed: %s",
                                      cudaGetErrorString(cudaGetLastError()));
