@@ -332,6 +332,15 @@ __device__ __forceinline__ void flag_status(unsigned *status, unsigned bits) {
     if (status) atomicOr(status, bits);
 }
 
+// 2^x by the hardware approximation (one instruction; relative error of a
+// few units in the last place of fp32, subnormal results flushed to zero):
+// the softmax exponentials, whose results feed bf16 / f16 MMA operands.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // mbarrier ------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));

@@ -89,12 +89,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return warp_mbar_wait(bar, parity, abort);
 }
 
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // Packed pairs of fp32 (one 64-bit register pair) for the two-wide FMA / add
 // of this architecture, and the three-input maximum: the softmax warps are
 // bound by instruction issue, so each score costs half an FMA, half an add,

@@ -253,8 +253,8 @@ __device__ __forceinline__ void swapped_chunks(Consumer<D> &cs, const uint32_t (
         }
         const bool up0 = ma > cs.m0 + kRescaleThreshold || (cs.m0 == -INFINITY && ma > -INFINITY);
         const bool up1 = mb > cs.m1 + kRescaleThreshold || (cs.m1 == -INFINITY && mb > -INFINITY);
-        const float a0 = up0 ? (cs.m0 == -INFINITY ? 0.f : exp2f(cs.m0 - ma)) : 1.f;
-        const float a1 = up1 ? (cs.m1 == -INFINITY ? 0.f : exp2f(cs.m1 - mb)) : 1.f;
+        const float a0 = up0 ? (cs.m0 == -INFINITY ? 0.f : fast_exp2(cs.m0 - ma)) : 1.f;
+        const float a1 = up1 ? (cs.m1 == -INFINITY ? 0.f : fast_exp2(cs.m1 - mb)) : 1.f;
         if (up0) cs.m0 = ma;
         if (up1) cs.m1 = mb;
         cs.l0 *= a0;
@@ -273,8 +273,8 @@ __device__ __forceinline__ void swapped_chunks(Consumer<D> &cs, const uint32_t (
     uint32_t pb0[NC], pb1[NC];
 #pragma unroll
     for (int n = 0; n < NC; ++n) {
-        const float p0 = exp2f(s[n][0] - ref0), p1 = exp2f(s[n][1] - ref1);
-        const float p2 = exp2f(s[n][2] - ref0), p3 = exp2f(s[n][3] - ref1);
+        const float p0 = fast_exp2(s[n][0] - ref0), p1 = fast_exp2(s[n][1] - ref1);
+        const float p2 = fast_exp2(s[n][2] - ref0), p3 = fast_exp2(s[n][3] - ref1);
         cs.l0 += p0 + p2;
         cs.l1 += p1 + p3;
         pb0[n] = movmatrix_trans(pack_f16x2(p0, p1));
@@ -867,8 +867,8 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                     if (__any_sync(0xffffffffu, up0 || up1)) {
                         const float nm0 = up0 ? mx0 : cs.m0;
                         const float nm1 = up1 ? mx1 : cs.m1;
-                        const float a0 = up0 ? (cs.m0 == -INFINITY ? 0.f : exp2f(cs.m0 - nm0)) : 1.f;
-                        const float a1 = up1 ? (cs.m1 == -INFINITY ? 0.f : exp2f(cs.m1 - nm1)) : 1.f;
+                        const float a0 = up0 ? (cs.m0 == -INFINITY ? 0.f : fast_exp2(cs.m0 - nm0)) : 1.f;
+                        const float a1 = up1 ? (cs.m1 == -INFINITY ? 0.f : fast_exp2(cs.m1 - nm1)) : 1.f;
                         cs.m0 = nm0;
                         cs.m1 = nm1;
                         cs.l0 *= a0;
@@ -886,10 +886,10 @@ __global__ void __launch_bounds__(kShortThreads, 2)
                     float pr[2][4];
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
-                        pr[nt][0] = exp2f(sacc[nt][0] - ref0);
-                        pr[nt][1] = exp2f(sacc[nt][1] - ref0);
-                        pr[nt][2] = exp2f(sacc[nt][2] - ref1);
-                        pr[nt][3] = exp2f(sacc[nt][3] - ref1);
+                        pr[nt][0] = fast_exp2(sacc[nt][0] - ref0);
+                        pr[nt][1] = fast_exp2(sacc[nt][1] - ref0);
+                        pr[nt][2] = fast_exp2(sacc[nt][2] - ref1);
+                        pr[nt][3] = fast_exp2(sacc[nt][3] - ref1);
                     }
                     cs.l0 += pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
                     cs.l1 += pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
