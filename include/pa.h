@@ -84,7 +84,10 @@ enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 };
  * run on the tensor-core kernel over a bf16 copy of their blocks when the
  * workspace has room for it (pa_fp8_staging_bytes), and on the split-KV
  * kernel in pieces of 64 / group query tokens otherwise.
- * pa_prefix_attention and pa_cascade_decode accept bf16 pools only.
+ * pa_prefix_attention and pa_cascade_decode decode the shared prefix's
+ * blocks into a bf16 staging copy in the workspace for their tensor-core
+ * prefix pass (see pa_cascade_fp8_staging_bytes); cascade decode's suffix
+ * pass runs on the fp8 split-KV kernel.
  */
 typedef struct pa_kv_desc {
     void *k_cache;
@@ -260,6 +263,18 @@ int pa_attention_no_alloc(const void *q, const pa_kv_desc *kv, const int32_t *bl
  */
 size_t pa_cascade_workspace_size(int32_t num_seqs, int32_t num_q_tokens, int32_t num_q_heads,
                                  int32_t num_kv_heads, int32_t head_dim, int32_t prefix_len);
+
+/*
+ * Extra workspace bytes, on top of pa_cascade_workspace_size, that
+ * pa_prefix_attention and pa_cascade_decode need on an fp8 (e4m3) pool: the
+ * prefix's ceil(prefix_len / block_size) blocks decoded to bf16 (exactly;
+ * the per-kv-head scales are applied by the kernel) for the tensor-core
+ * prefix pass, and their block list.  0 for an empty prefix; bf16 pools
+ * need none.  A smaller workspace is refused with PA_ERR_WORKSPACE.
+ * Returns 0 for invalid sizes.
+ */
+size_t pa_cascade_fp8_staging_bytes(int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t block_size, int32_t prefix_len);
 
 /*
  * Shared-prefix ("multi-query") attention of cascade inference ([AI]

@@ -32,7 +32,7 @@ PA_DEV_BAD_METADATA, PA_DEV_BAD_BLOCK, PA_DEV_BAD_SLOT, PA_DEV_WAIT_TIMEOUT, \
     PA_DEV_PLAN_OVERFLOW = 0x1, 0x2, 0x4, 0x8, 0x10
 
 EXPORTED = ["pa_write_kv", "pa_attention_workspace_size", "pa_attention", "pa_attention_ex",
-            "pa_write_kv_attention",
+            "pa_write_kv_attention", "pa_cascade_fp8_staging_bytes",
             "pa_merge_states", "pa_cascade_workspace_size", "pa_prefix_attention",
             "pa_cascade_decode", "pa_validate_metadata", "pa_last_error_message",
             "pa_status_string", "pa_read_device_status", "pa_set_profile_events",
@@ -84,6 +84,7 @@ def _declare(lib):
                                    P, sz, P], ctypes.c_int),
         "pa_merge_states": ([P, P, P, P, i32, i32, i32, P, P, P], ctypes.c_int),
         "pa_cascade_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
+        "pa_cascade_fp8_staging_bytes": ([i32, i32, i32, i32], sz),
         "pa_prefix_attention": ([P, KV, P, i32, i32, i32, f32, P, P, P, sz, P], ctypes.c_int),
         "pa_cascade_decode": ([P, KV, P, i32, P, i32, P, P, P, i32, i32, i32, f32, P, P, P, sz,
                                P], ctypes.c_int),
@@ -215,6 +216,20 @@ def cascade_workspace_size(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, he
                                                head_dim, prefix_len))
 
 
+def cascade_fp8_staging_bytes(num_kv_heads, head_dim, block_size, prefix_len) -> int:
+    return int(lib().pa_cascade_fp8_staging_bytes(num_kv_heads, head_dim, block_size,
+                                                  int(prefix_len)))
+
+
+def _cascade_need(kv, num_seqs, T, hq, prefix_len) -> int:
+    need = cascade_workspace_size(num_seqs, T, hq, kv.num_kv_heads, kv.head_dim, prefix_len)
+    if kv.kv_dtype == PA_KV_FP8_E4M3:
+        # the workspace's tail holds the prefix decoded to bf16
+        need = ((need + 255) // 256) * 256 + cascade_fp8_staging_bytes(
+            kv.num_kv_heads, kv.head_dim, kv.block_size, prefix_len)
+    return need
+
+
 def alloc_workspace(nbytes: int, device=None) -> torch.Tensor:
     """Device workspace owned by torch (256-byte aligned by the allocator)."""
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device or "cuda")
@@ -304,13 +319,15 @@ def pa_merge_states(o_a, lse_a, o_b, lse_b, out, lse_out=None, stream=None):
 
 
 def pa_prefix_attention(q, k_cache, v_cache, prefix_blocks, prefix_len, scale, out, lse=None,
-                        workspace=None, stream=None):
+                        workspace=None, stream=None, k_scale=None, v_scale=None):
+    """Shared-prefix attention; an fp8 pool takes k_scale / v_scale (fp32
+    [Hkv]) and a workspace with room for the prefix's bf16 copy."""
     _need(q, "q", torch.bfloat16)
     _need(out, "out", torch.bfloat16)
     _need(prefix_blocks, "prefix_blocks", torch.int32)
-    kv = kv_desc(k_cache, v_cache)
+    kv = kv_desc(k_cache, v_cache, k_scale, v_scale)
     T, hq, _ = q.shape
-    need = cascade_workspace_size(1, T, hq, kv.num_kv_heads, kv.head_dim, prefix_len)
+    need = _cascade_need(kv, 1, T, hq, prefix_len)
     if workspace is None or workspace.numel() < need:
         workspace = alloc_workspace(need, q.device)
     _check(lib().pa_prefix_attention(_ptr(q), ctypes.byref(kv), _ptr(prefix_blocks),
@@ -322,17 +339,19 @@ def pa_prefix_attention(q, k_cache, v_cache, prefix_blocks, prefix_len, scale, o
 
 def pa_cascade_decode(q, k_cache, v_cache, prefix_blocks, prefix_len, block_tables,
                       query_start_loc, context_lens, seq_lens, scale, out, lse=None,
-                      workspace=None, stream=None):
+                      workspace=None, stream=None, k_scale=None, v_scale=None):
+    """Cascade decode; an fp8 pool takes k_scale / v_scale (fp32 [Hkv]) and a
+    workspace with room for the prefix's bf16 copy."""
     _need(q, "q", torch.bfloat16)
     _need(out, "out", torch.bfloat16)
     for name, t in (("prefix_blocks", prefix_blocks), ("block_tables", block_tables),
                     ("query_start_loc", query_start_loc), ("context_lens", context_lens),
                     ("seq_lens", seq_lens)):
         _need(t, name, torch.int32)
-    kv = kv_desc(k_cache, v_cache)
+    kv = kv_desc(k_cache, v_cache, k_scale, v_scale)
     T, hq, _ = q.shape
     B = int(seq_lens.shape[0])
-    need = cascade_workspace_size(B, T, hq, kv.num_kv_heads, kv.head_dim, prefix_len)
+    need = _cascade_need(kv, B, T, hq, prefix_len)
     if workspace is None or workspace.numel() < need:
         workspace = alloc_workspace(need, q.device)
     _check(lib().pa_cascade_decode(_ptr(q), ctypes.byref(kv), _ptr(prefix_blocks),

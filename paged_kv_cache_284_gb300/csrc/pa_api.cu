@@ -291,6 +291,66 @@ int make_staging(Staging *st, const pa_kv_desc *kv, uint8_t *ws, size_t used, si
     return rc;
 }
 
+// Cascade decode on an e4m3 pool: the shared prefix decoded to bf16 for the
+// tensor-core prefix pass, in the workspace beyond the call's own layout:
+// the identity block list ident[k] = k (n int32), then n staging blocks of K
+// and of V.  n = 0: a bf16 pool or an empty prefix (nothing staged).
+struct PrefixStage {
+    int n = 0;
+    int32_t *ident = nullptr;
+    Staging stg;
+};
+
+size_t prefix_stage_bytes(int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                          int32_t prefix_len) {
+    const int64_t n = (static_cast<int64_t>(prefix_len) + block_size - 1) / block_size;
+    if (n == 0) return 0;
+    const size_t blk = static_cast<size_t>(num_kv_heads) * block_size * head_dim * 2;
+    return align256(sizeof(int32_t) * static_cast<size_t>(n)) +
+           2 * align256(static_cast<size_t>(n) * blk) + 768;
+}
+
+int make_prefix_stage(PrefixStage *ps, const pa_kv_desc *kv, int32_t prefix_len, uint8_t *ws,
+                      size_t used, size_t total) {
+    ps->n = 0;
+    if (kv->kv_dtype != PA_KV_FP8_E4M3 || prefix_len == 0) return PA_OK;
+    const int n = (prefix_len + kv->block_size - 1) / kv->block_size;
+    const size_t start = align256(used);
+    const size_t need =
+        start + prefix_stage_bytes(kv->num_kv_heads, kv->head_dim, kv->block_size, prefix_len);
+    if (total < need)
+        return fail(PA_ERR_WORKSPACE,
+                    "an e4m3 pool's shared prefix is decoded to bf16 in the workspace: it needs "
+                    "%zu bytes (pa_cascade_workspace_size + pa_cascade_fp8_staging_bytes), got %zu",
+                    need, total);
+    ps->ident = reinterpret_cast<int32_t *>(ws + start);
+    int rc = make_staging(&ps->stg, kv, ws, start + align256(sizeof(int32_t) * n), total);
+    if (rc != PA_OK) return fail(rc, "prefix staging map failed");
+    if (ps->stg.cap < n) return fail(PA_ERR_WORKSPACE, "prefix staging area too small");
+    ps->n = n;
+    return PA_OK;
+}
+
+// Decodes the prefix into the staging area (a launch on `s`) and points the
+// prefix pass at it: the identity list, the staging blocks and the pool's
+// scales.  The pass's K and V tensor maps become *tk and *tv.
+int stage_prefix(const PrefixStage &ps, const pa_kv_desc *kv, const int32_t *prefix_blocks,
+                 LongParams *lp, const CUtensorMap **tk, const CUtensorMap **tv,
+                 DeviceInfo *dev, cudaStream_t s) {
+    if (ps.n == 0) return PA_OK;
+    const int rc = launch_stage_prefix_fp8(kv, prefix_blocks, ps.n, ps.ident, ps.stg.k,
+                                           ps.stg.v, dev->status, 2 * dev->sms, s);
+    if (rc != PA_OK) return fail(rc, "prefix staging launch failed");
+    lp->block_tables = ps.ident;
+    lp->num_blocks = ps.stg.cap;
+    lp->kv_rows = ps.stg.cap * kv->num_kv_heads * kv->block_size;
+    lp->k_scale = kv->k_scale;
+    lp->v_scale = kv->v_scale;
+    *tk = &ps.stg.tk;
+    *tv = &ps.stg.tv;
+    return PA_OK;
+}
+
 int make_maps(StepMaps *m, const void *q, const pa_kv_desc *kv, int tokens, int heads) {
     const int group = heads / kv->num_kv_heads;
     const bool fp8 = kv->kv_dtype == PA_KV_FP8_E4M3;
@@ -353,6 +413,7 @@ LongParams prefix_params(const pa_kv_desc *kv, const int32_t *prefix_blocks, int
 struct CascadeArgs {
     const int32_t *prefix_blocks;
     int32_t prefix_len;
+    const PrefixStage *ps;  // an e4m3 pool's prefix, decoded to bf16 (ps->n = 0: none)
     float *prefix_o, *prefix_lse;  // prefix split states
     float *suffix_o, *suffix_lse;  // suffix state per row, fp32
 };
@@ -493,6 +554,11 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
         LongParams cp = prefix_params(kv, casc->prefix_blocks, casc->prefix_len, T, Hq, scale,
                                       q_tiles, nsplit, split_keys_p, casc->prefix_o,
                                       casc->prefix_lse, dev);
+        // an e4m3 pool: the prefix decoded to bf16 first (after the plan; the
+        // first prefix grid waits for it)
+        const CUtensorMap *ptk = &maps.k, *ptv = &maps.v;
+        rc = stage_prefix(*casc->ps, kv, casc->prefix_blocks, &cp, &ptk, &ptv, dev, s);
+        if (rc != PA_OK) return rc;
         cp.hdr = hdr;
         cp.states_only = 1;
         cp.dynamic = 1;
@@ -502,20 +568,20 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
         LongParams c1 = cp;
         c1.wait_start = 1;
         c1.first_ctas = -1;
-        rc = launch_long(c1, maps.q, maps.k, maps.v, D, g1, s);
+        rc = launch_long(c1, maps.q, *ptk, *ptv, D, g1, s);
         if (rc != PA_OK) return fail(rc, "prefix kernel launch failed: %s",
                                      cudaGetErrorString(cudaGetLastError()));
         sp.no_start_wait = 1;
         sp.test_stall = 0;
         sp.out_f32 = casc->suffix_o;
         sp.lse = casc->suffix_lse;
-        rc = launch_short(sp, maps.k, maps.v, D, false, short_grid, s);
+        rc = launch_short(sp, maps.k, maps.v, D, fp8, short_grid, s);
         if (rc != PA_OK) return fail(rc, "split-KV kernel launch failed: %s",
                                      cudaGetErrorString(cudaGetLastError()));
         LongParams c2 = cp;
         c2.overlap_prev = 1;
         c2.first_ctas = g1;
-        rc = launch_long(c2, maps.q, maps.k, maps.v, D, n_prefix, s);
+        rc = launch_long(c2, maps.q, *ptk, *ptv, D, n_prefix, s);
         if (rc != PA_OK) return fail(rc, "prefix kernel launch failed: %s",
                                      cudaGetErrorString(cudaGetLastError()));
         PrefixFoldParams f{};
@@ -665,7 +731,8 @@ int common_checks(const void *q, const pa_kv_desc *kv, int32_t num_q_tokens, int
 
 int run_prefix(const void *q, const pa_kv_desc *kv, const int32_t *prefix_blocks, int32_t prefix_len,
                int32_t T, int32_t Hq, float scale, void *out, float *lse, uint8_t *ws,
-               const WsLayout &L, const StepMaps &maps, DeviceInfo *dev, cudaStream_t s) {
+               const WsLayout &L, const StepMaps &maps, const PrefixStage &ps, DeviceInfo *dev,
+               cudaStream_t s) {
     const int group = Hq / kv->num_kv_heads;
     int q_tiles, nsplit, split_keys;
     prefix_plan(T, prefix_len, kv->num_kv_heads, group, dev->sms, &q_tiles, &nsplit, &split_keys);
@@ -676,8 +743,11 @@ int run_prefix(const void *q, const pa_kv_desc *kv, const int32_t *prefix_blocks
                                   reinterpret_cast<float *>(ws + L.prefix_lse), dev);
     lp.out = static_cast<__nv_bfloat16 *>(out);
     lp.lse = lse;
+    const CUtensorMap *tk = &maps.k, *tv = &maps.v;
+    int rc = stage_prefix(ps, kv, prefix_blocks, &lp, &tk, &tv, dev, s);
+    if (rc != PA_OK) return rc;
     const int grid = kv->num_kv_heads * q_tiles * nsplit;
-    int rc = launch_long(lp, maps.q, maps.k, maps.v, kv->head_dim, grid, s);
+    rc = launch_long(lp, maps.q, *tk, *tv, kv->head_dim, grid, s);
     if (rc != PA_OK) return fail(rc, "prefix kernel launch failed");
     if (nsplit > 1) {
         PrefixFoldParams f{};
@@ -964,8 +1034,6 @@ int pa_prefix_attention(const void *q, const pa_kv_desc *kv, const int32_t *pref
     g_err[0] = 0;
     int rc = common_checks(q, kv, num_q_tokens, num_q_heads, scale, out, workspace);
     if (rc != PA_OK) return rc;
-    if (kv->kv_dtype != PA_KV_BF16)
-        return fail(PA_ERR_UNSUPPORTED, "prefix attention is built for bf16 KV pools only");
     if (prefix_len < 0) return fail(PA_ERR_INVALID_ARG, "prefix_len < 0");
     if (prefix_len > 0 && !prefix_blocks) return fail(PA_ERR_INVALID_ARG, "prefix_blocks is NULL");
     if (num_q_tokens == 0) return PA_OK;
@@ -977,12 +1045,16 @@ int pa_prefix_attention(const void *q, const pa_kv_desc *kv, const int32_t *pref
     if (!workspace || workspace_bytes < L.total)
         return fail(PA_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", L.total,
                     workspace_bytes);
+    PrefixStage ps;
+    if ((rc = make_prefix_stage(&ps, kv, prefix_len, static_cast<uint8_t *>(workspace), L.total,
+                                workspace_bytes)) != PA_OK)
+        return rc;
     DeviceInfo *dev;
     if ((rc = device_info(&dev)) != PA_OK) return rc;
     StepMaps maps;
     if ((rc = make_maps(&maps, q, kv, num_q_tokens, num_q_heads)) != PA_OK) return rc;
     return run_prefix(q, kv, prefix_blocks, prefix_len, num_q_tokens, num_q_heads, scale, out,
-                      lse, static_cast<uint8_t *>(workspace), L, maps, dev,
+                      lse, static_cast<uint8_t *>(workspace), L, maps, ps, dev,
                       static_cast<cudaStream_t>(stream));
 }
 
@@ -995,8 +1067,6 @@ int pa_cascade_decode(const void *q, const pa_kv_desc *kv, const int32_t *prefix
     g_err[0] = 0;
     int rc = common_checks(q, kv, num_q_tokens, num_q_heads, scale, out, workspace);
     if (rc != PA_OK) return rc;
-    if (kv->kv_dtype != PA_KV_BF16)
-        return fail(PA_ERR_UNSUPPORTED, "cascade decode is built for bf16 KV pools only");
     if (num_q_heads / kv->num_kv_heads > kShortMaxRows)
         return fail(PA_ERR_UNSUPPORTED, "cascade decode: group size above %d not built",
                     kShortMaxRows);
@@ -1015,14 +1085,18 @@ int pa_cascade_decode(const void *q, const pa_kv_desc *kv, const int32_t *prefix
     if (!workspace || workspace_bytes < L.total)
         return fail(PA_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", L.total,
                     workspace_bytes);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    PrefixStage ps;
+    if ((rc = make_prefix_stage(&ps, kv, prefix_len, ws, L.total, workspace_bytes)) != PA_OK)
+        return rc;
     DeviceInfo *dev;
     if ((rc = device_info(&dev)) != PA_OK) return rc;
     StepMaps maps;
     if ((rc = make_maps(&maps, q, kv, num_q_tokens, num_q_heads)) != PA_OK) return rc;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
     CascadeArgs casc;
     casc.prefix_blocks = prefix_blocks;
     casc.prefix_len = prefix_len;
+    casc.ps = &ps;
     casc.prefix_o = reinterpret_cast<float *>(ws + L.prefix_o);
     casc.prefix_lse = reinterpret_cast<float *>(ws + L.prefix_lse);
     casc.suffix_o = reinterpret_cast<float *>(ws + L.extra_o);
@@ -1031,6 +1105,12 @@ int pa_cascade_decode(const void *q, const pa_kv_desc *kv, const int32_t *prefix
                     seq_lens, num_seqs, num_q_tokens, num_q_heads, scale, out, lse, ws, L,
                     kShortMaxRows, 0, &casc, true, maps, Staging(), dev,
                     static_cast<cudaStream_t>(stream));
+}
+
+size_t pa_cascade_fp8_staging_bytes(int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t block_size, int32_t prefix_len) {
+    if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || prefix_len < 0) return 0;
+    return prefix_stage_bytes(num_kv_heads, head_dim, block_size, prefix_len);
 }
 
 int pa_validate_metadata(const int32_t *block_tables, int32_t max_blocks_per_seq,

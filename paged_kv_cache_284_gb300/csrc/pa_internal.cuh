@@ -278,6 +278,11 @@ int launch_write_kv(const void *k, const void *v, const int64_t *slots, int num_
 int launch_stage_fp8(const pa_kv_desc *kv, const int32_t *block_tables, int32_t bt_stride,
                      const PlanHeader *hdr, const int *stage_base, const int *stage_list,
                      void *stage_k, void *stage_v, unsigned *status, int grid, cudaStream_t s);
+// The shared prefix's n e4m3 blocks decoded to bf16 staging blocks 0..n-1
+// (cascade decode on an e4m3 pool); ident[k] = k is the staged block list.
+int launch_stage_prefix_fp8(const pa_kv_desc *kv, const int32_t *prefix_blocks, int n,
+                            int32_t *ident, void *stage_k, void *stage_v, unsigned *status,
+                            int grid, cudaStream_t s);
 int launch_plan(const PlanParams &p, cudaStream_t s);
 int launch_short(const ShortParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                  int head_dim, bool fp8, int grid, cudaStream_t s);

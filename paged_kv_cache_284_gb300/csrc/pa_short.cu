@@ -323,8 +323,8 @@ __device__ __forceinline__ void swapped_chunks(Consumer<D> &cs, const uint32_t (
 
 // Item epilogue of a swapped fp8 item: row sums over the 8 lanes of a row,
 // the 4 consumer warps merged through the stage buffer, then warp 0 writes
-// rows 2t and 2t+1 (output or partial state).  Cascade calls take bf16 pools
-// only, so the fp32 state output is not needed here.
+// rows 2t and 2t+1 (output, fp32 state for cascade decode, or partial
+// state).
 template <int D>
 __device__ __forceinline__ void swapped_epilogue(Consumer<D> &cs, const ShortParams &p,
                                                  float *scratch, int lane, int warp) {
@@ -390,7 +390,14 @@ __device__ __forceinline__ void swapped_epilogue(Consumer<D> &cs, const ShortPar
         const int tok = cs.tok0 + r / p.group;
         const int hq = cs.h * p.group + r % p.group;
         const int64_t row = static_cast<int64_t>(tok) * p.num_q_heads + hq;
-        if (cs.nsplit == 1) {
+        if (cs.nsplit == 1 && p.out_f32) {
+            float *dst = p.out_f32 + row * D;
+#pragma unroll
+            for (int cc = 0; cc < D / 16; ++cc)
+                __stcg(reinterpret_cast<float2 *>(dst + cc * 16 + 2 * g),
+                       make_float2(cs.o[cc][half] * inv, cs.o[cc][2 + half] * inv));
+            if (p.lse && g == 0) p.lse[row] = lse_v;
+        } else if (cs.nsplit == 1) {
             uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + row * D);
 #pragma unroll
             for (int cc = 0; cc < D / 16; ++cc)

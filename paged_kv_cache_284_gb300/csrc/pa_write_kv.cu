@@ -5,6 +5,8 @@
 // Pure HBM copy: each thread moves one 16-byte piece of one (token, kv head)
 // row for K and the same piece for V, so a warp covers whole 16-byte sectors
 // of the destination rows.
+#include <algorithm>
+
 #include <cuda_fp8.h>
 
 #include "pa_internal.cuh"
@@ -132,12 +134,47 @@ int launch_write_kv(const void *k, const void *v, const int64_t *slots, int num_
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+// Decodes e4m3 block src of the pool into bf16 staging block k (exact: every
+// e4m3 value is a bf16 value; the per-kv-head scales stay with the
+// attention kernel), the block's threads striding over its 16-code pieces.
+__device__ __forceinline__ void decode_block(const uint4 *__restrict__ kc8,
+                                             const uint4 *__restrict__ vc8, int64_t src,
+                                             int pieces_per_block, int64_t k,
+                                             uint4 *__restrict__ sk, uint4 *__restrict__ sv) {
+    for (int q = threadIdx.x; q < pieces_per_block; q += blockDim.x) {
+        // 16 codes -> 16 bf16 (two 16-byte pieces)
+        const uint4 ck = __ldg(kc8 + src * pieces_per_block + q);
+        const uint4 cv = __ldg(vc8 + src * pieces_per_block + q);
+        uint4 out[4];
+        const uint32_t wk[4] = {ck.x, ck.y, ck.z, ck.w}, wv[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            uint32_t k0, k1, v0, v1;
+            e4m3x4_to_f16x2x2(wk[w], k0, k1);
+            e4m3x4_to_f16x2x2(wv[w], v0, v1);
+            const __half2 hk0 = *reinterpret_cast<__half2 *>(&k0), hk1 = *reinterpret_cast<__half2 *>(&k1);
+            const __half2 hv0 = *reinterpret_cast<__half2 *>(&v0), hv1 = *reinterpret_cast<__half2 *>(&v1);
+            const float2 fk0 = __half22float2(hk0), fk1 = __half22float2(hk1);
+            const float2 fv0 = __half22float2(hv0), fv1 = __half22float2(hv1);
+            // out[0..1]: K (8 bf16 each), out[2..3]: V
+            reinterpret_cast<uint32_t *>(&out[w >> 1])[(w & 1) * 2] = pack_bf16x2(fk0.x, fk0.y);
+            reinterpret_cast<uint32_t *>(&out[w >> 1])[(w & 1) * 2 + 1] = pack_bf16x2(fk1.x, fk1.y);
+            reinterpret_cast<uint32_t *>(&out[2 + (w >> 1)])[(w & 1) * 2] = pack_bf16x2(fv0.x, fv0.y);
+            reinterpret_cast<uint32_t *>(&out[2 + (w >> 1)])[(w & 1) * 2 + 1] = pack_bf16x2(fv1.x, fv1.y);
+        }
+        const int64_t dst = (k * pieces_per_block + q) * 2;
+        sk[dst] = out[0];
+        sk[dst + 1] = out[1];
+        sv[dst] = out[2];
+        sv[dst + 1] = out[3];
+    }
+}
+
 // Staging copy of the e4m3 blocks of long requests for the tensor-core
 // kernel: staging block k of staged request b (k = stage_base[b] + j) holds
-// block j of b's table decoded to bf16 (exact: every e4m3 value is a bf16
-// value; the per-kv-head scales are applied by the attention kernel).
-// Grid-stride over staging blocks; thread 0 finds the request of a block by
-// binary search over the staged requests' first blocks.
+// block j of b's table decoded to bf16.  Grid-stride over staging blocks;
+// thread 0 finds the request of a block by binary search over the staged
+// requests' first blocks.
 __global__ void __launch_bounds__(256) stage_fp8_kernel(
     const uint4 *__restrict__ kc8, const uint4 *__restrict__ vc8, int num_blocks,
     int pieces_per_block, const int32_t *__restrict__ bt, int bt_stride, const PlanHeader *hdr,
@@ -165,34 +202,7 @@ __global__ void __launch_bounds__(256) stage_fp8_kernel(
             s_src = src;
         }
         __syncthreads();
-        const int64_t src = s_src;
-        for (int q = threadIdx.x; q < pieces_per_block; q += blockDim.x) {
-            // 16 codes -> 16 bf16 (two 16-byte pieces)
-            const uint4 ck = __ldg(kc8 + src * pieces_per_block + q);
-            const uint4 cv = __ldg(vc8 + src * pieces_per_block + q);
-            uint4 out[4];
-            const uint32_t wk[4] = {ck.x, ck.y, ck.z, ck.w}, wv[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                uint32_t k0, k1, v0, v1;
-                e4m3x4_to_f16x2x2(wk[w], k0, k1);
-                e4m3x4_to_f16x2x2(wv[w], v0, v1);
-                const __half2 hk0 = *reinterpret_cast<__half2 *>(&k0), hk1 = *reinterpret_cast<__half2 *>(&k1);
-                const __half2 hv0 = *reinterpret_cast<__half2 *>(&v0), hv1 = *reinterpret_cast<__half2 *>(&v1);
-                const float2 fk0 = __half22float2(hk0), fk1 = __half22float2(hk1);
-                const float2 fv0 = __half22float2(hv0), fv1 = __half22float2(hv1);
-                // out[0..1]: K (8 bf16 each), out[2..3]: V
-                reinterpret_cast<uint32_t *>(&out[w >> 1])[(w & 1) * 2] = pack_bf16x2(fk0.x, fk0.y);
-                reinterpret_cast<uint32_t *>(&out[w >> 1])[(w & 1) * 2 + 1] = pack_bf16x2(fk1.x, fk1.y);
-                reinterpret_cast<uint32_t *>(&out[2 + (w >> 1)])[(w & 1) * 2] = pack_bf16x2(fv0.x, fv0.y);
-                reinterpret_cast<uint32_t *>(&out[2 + (w >> 1)])[(w & 1) * 2 + 1] = pack_bf16x2(fv1.x, fv1.y);
-            }
-            const int64_t dst = (static_cast<int64_t>(k) * pieces_per_block + q) * 2;
-            sk[dst] = out[0];
-            sk[dst + 1] = out[1];
-            sv[dst] = out[2];
-            sv[dst + 1] = out[3];
-        }
+        decode_block(kc8, vc8, s_src, pieces_per_block, k, sk, sv);
         __syncthreads();
     }
 }
@@ -209,6 +219,39 @@ int launch_stage_fp8(const pa_kv_desc *kv, const int32_t *block_tables, int32_t 
         static_cast<const uint4 *>(kv->v_cache), kv->num_blocks, pieces, block_tables, bt_stride,
         hdr, stage_base, stage_list, static_cast<uint4 *>(stage_k), static_cast<uint4 *>(stage_v),
         status);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// Cascade decode on an e4m3 pool: the shared prefix's n blocks (list[k],
+// k < n) decoded to bf16 staging blocks 0..n-1 for the tensor-core prefix
+// pass, which then reads them through the identity list ident[k] = k.
+__global__ void __launch_bounds__(256) stage_prefix_fp8_kernel(
+    const uint4 *__restrict__ kc8, const uint4 *__restrict__ vc8, int num_blocks,
+    int pieces_per_block, const int32_t *__restrict__ list, int n, int32_t *__restrict__ ident,
+    uint4 *__restrict__ sk, uint4 *__restrict__ sv, unsigned *status) {
+    pdl_wait();  // the list may come from the previous kernel, which may still read the cache
+    pdl_trigger();
+    for (int k = blockIdx.x; k < n; k += gridDim.x) {
+        int64_t src = __ldg(list + k);
+        if (src < 0 || src >= num_blocks) {
+            if (threadIdx.x == 0) flag_status(status, PA_DEV_BAD_BLOCK);
+            src = src < 0 ? 0 : num_blocks - 1;
+        }
+        if (threadIdx.x == 0) ident[k] = k;
+        decode_block(kc8, vc8, src, pieces_per_block, k, sk, sv);
+    }
+}
+
+int launch_stage_prefix_fp8(const pa_kv_desc *kv, const int32_t *prefix_blocks, int n,
+                            int32_t *ident, void *stage_k, void *stage_v, unsigned *status,
+                            int grid, cudaStream_t s) {
+    if (n <= 0) return PA_OK;
+    const int pieces = kv->num_kv_heads * kv->block_size * kv->head_dim / 16;
+    PdlLaunch l(static_cast<unsigned>(std::max(1, std::min(grid, n))), 256, 0, s);
+    const cudaError_t e = launch_kernel(
+        l, stage_prefix_fp8_kernel, static_cast<const uint4 *>(kv->k_cache),
+        static_cast<const uint4 *>(kv->v_cache), kv->num_blocks, pieces, prefix_blocks, n, ident,
+        static_cast<uint4 *>(stage_k), static_cast<uint4 *>(stage_v), status);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

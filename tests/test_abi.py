@@ -130,11 +130,20 @@ def test_fp8_descriptor_is_checked_on_host():
     ]
     for kv, want in cases:
         assert lib.pa_write_kv(fake, fake, fake, 4, ctypes.byref(kv), None) == want
-    # prefix attention and cascade decode take bf16 pools only
+    # on an fp8 pool, prefix attention and cascade decode need room for the
+    # prefix's bf16 copy beyond their layout: refused on the host without it
     kv = pk.KVDesc(1 << 20, 1 << 21, 100, 16, 8, 128, pk.PA_KV_FP8_E4M3, 0, 1 << 22, 1 << 22)
+    base = pk.cascade_workspace_size(1, 4, 32, 8, 128, 64)
+    extra = pk.cascade_fp8_staging_bytes(8, 128, 16, 64)
+    assert base > 0 and extra >= 4 * 2 * (8 * 16 * 128 * 2)   # 4 blocks of K and V in bf16
     rc = lib.pa_prefix_attention(fake, ctypes.byref(kv), fake, 64, 4, 32, 0.1, fake, None,
-                                 ctypes.c_void_p(1 << 23), 1 << 30, None)
-    assert rc == pk.PA_ERR_UNSUPPORTED
+                                 ctypes.c_void_p(1 << 23), base, None)
+    assert rc == pk.PA_ERR_WORKSPACE
+    rc = lib.pa_cascade_decode(fake, ctypes.byref(kv), fake, 64, fake, 8, fake, fake, fake, 4, 4,
+                               32, 0.1, fake, None, ctypes.c_void_p(1 << 23),
+                               pk.cascade_workspace_size(4, 4, 32, 8, 128, 64), None)
+    assert rc == pk.PA_ERR_WORKSPACE
+    assert pk.cascade_fp8_staging_bytes(8, 128, 16, 0) == 0
 
 
 def test_kv_descriptor_layout():

@@ -139,3 +139,61 @@ def test_fp8_partial_staging_splits_long_rows_between_the_paths():
     pool8 = workloads.fp8_pool_like(pool, 7022)
     run_and_check_fp8(pool8, [step], staging_blocks=first)
     assert plan_header(gpu_attend_fp8.last_workspace)["num_staged"] == 1
+
+
+@pytest.mark.parametrize("prefix_len,hq,hkv", [(0, 32, 8), (16, 32, 8), (512, 32, 8),
+                                               (2048, 32, 8), (512, 32, 2)])
+def test_fp8_cascade_decode_equals_full_attention(prefix_len, hq, hkv):
+    """Cascade decode on an e4m3 pool (the prefix decoded to bf16 for the
+    tensor-core prefix pass, the suffixes on the fp8 split-KV kernel writing
+    fp32 states, the fold merging both) equals the oracle's fp8 attention
+    over the full tables.  Group 4 takes the operand-swapped suffix path,
+    group 16 the general one."""
+    pool, (step,) = workloads.cascade(seed=7200 + prefix_len + hkv, num_seqs=9,
+                                      prefix_len=prefix_len, suffix=(1, 300), num_q_heads=hq,
+                                      num_kv_heads=hkv)
+    pool8 = workloads.fp8_pool_like(pool, 7201)
+    kc, vc, ks, vs = fp8_dev(pool8)
+    gpu_write_fp8(step, kc, vc, ks, vs)
+    sk, sv = pool8.k_scale.numpy(), pool8.v_scale.numpy()
+    kb, vb = oracle.write_kv_fp8(step.k, step.v, step.slot_mapping, codes(pool8.k_cache),
+                                 codes(pool8.v_cache), sk, sv)
+    q = step.q.to(DEV)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    pk.pa_cascade_decode(q, kc, vc, step.prefix_blocks.to(DEV), step.prefix_len,
+                         step.suffix_block_tables.to(DEV), step.query_start_loc.to(DEV),
+                         step.suffix_context_lens.to(DEV), step.suffix_seq_lens.to(DEV),
+                         step.scale, out, lse, k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert np.array_equal(codes(kc), kb) and np.array_equal(codes(vc), vb)
+    ro, rl = oracle.attention_fp8(step.q, kb, vb, sk, sv, step.block_tables,
+                                  step.query_start_loc, step.context_lens, step.seq_lens,
+                                  step.scale)
+    assert_attention_close(out, lse, ro, rl, f"fp8 cascade, prefix {prefix_len}, group {hq // hkv}")
+    assert_status_clean()
+
+
+def test_fp8_prefix_attention_matches_oracle():
+    """Shared-prefix attention on an e4m3 pool: every query row over all
+    prefix keys, against the oracle's fp8 attention with each row a request
+    whose table is the prefix (context prefix_len - 1, so no key is masked)."""
+    pool, (step,) = workloads.cascade(seed=7210, num_seqs=12, prefix_len=704, suffix=(1, 50))
+    pool8 = workloads.fp8_pool_like(pool, 7211)
+    kc, vc, ks, vs = fp8_dev(pool8)
+    q = step.q.to(DEV)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    pk.pa_prefix_attention(q, kc, vc, step.prefix_blocks.to(DEV), step.prefix_len, step.scale,
+                           out, lse, k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    T = step.num_q_tokens
+    bt = step.prefix_blocks.view(1, -1).repeat(T, 1).contiguous()
+    qsl = torch.arange(T + 1, dtype=torch.int32)
+    ctx = torch.full((T,), step.prefix_len - 1, dtype=torch.int32)
+    sl = torch.full((T,), step.prefix_len, dtype=torch.int32)
+    ro, rl = oracle.attention_fp8(step.q, codes(pool8.k_cache), codes(pool8.v_cache),
+                                  pool8.k_scale.numpy(), pool8.v_scale.numpy(), bt, qsl, ctx, sl,
+                                  step.scale)
+    assert_attention_close(out, lse, ro, rl, "fp8 prefix attention")
+    assert_status_clean()
