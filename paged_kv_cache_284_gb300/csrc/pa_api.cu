@@ -542,13 +542,13 @@ int run_step(const void *q, const pa_kv_desc *kv, const int32_t *block_tables, i
         // completes after both.  The split-KV grid writes
         // each row's suffix state in fp32; the fold kernel merges it with the
         // prefix split states into out and lse.
-        // The prefix pass (compute) is the long pole: its items are cut for
-        // one round on about 42 % of the SMs (the first grid takes them all),
-        // the split-KV grid streams the suffixes on the rest.  Measured on
-        // 64 requests x an 8192-token prefix: 66.2 us, against 69.4 us with
-        // 8-tile items pulled by a third of the SMs and 73.7 us with 96 SMs.
+        // The prefix pass's items are cut for one round on about 36 % of the
+        // SMs (the first grid takes them all); the split-KV grid streams the
+        // suffixes on the rest.  Measured on 64 requests x an 8192-token
+        // prefix, us per call by share: 28 % 73.9 (too few splits), 32 %
+        // 63.4, 36 % 63.1-63.5, 42 % 64.6, 48 % 64.5, 54 % 67.4.
         int q_tiles, nsplit, split_keys_p;
-        const int prefix_sms = std::max(1, (dev->sms * 42 + 50) / 100);
+        const int prefix_sms = std::max(1, (dev->sms * 36 + 50) / 100);
         prefix_plan(T, casc->prefix_len, kv->num_kv_heads, group, prefix_sms, &q_tiles, &nsplit,
                     &split_keys_p);
         LongParams cp = prefix_params(kv, casc->prefix_blocks, casc->prefix_len, T, Hq, scale,
