@@ -314,7 +314,8 @@ int make_prefix_stage(PrefixStage *ps, const pa_kv_desc *kv, int32_t prefix_len,
                       size_t used, size_t total) {
     ps->n = 0;
     if (kv->kv_dtype != PA_KV_FP8_E4M3 || prefix_len == 0) return PA_OK;
-    const int n = (prefix_len + kv->block_size - 1) / kv->block_size;
+    const int n = static_cast<int>((static_cast<int64_t>(prefix_len) + kv->block_size - 1) /
+                                   kv->block_size);
     const size_t start = align256(used);
     const size_t need =
         start + prefix_stage_bytes(kv->num_kv_heads, kv->head_dim, kv->block_size, prefix_len);
