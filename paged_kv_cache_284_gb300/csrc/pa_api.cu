@@ -426,6 +426,16 @@ struct NewRows {
     int32_t num_tokens;
 };
 
+// Checks of pa_write_kv's arguments; num_tokens == 0 needs no pointers.
+int check_new_rows(const NewRows &nr) {
+    if (nr.num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
+    if (nr.num_tokens == 0) return PA_OK;
+    if (!nr.k || !nr.v || !nr.slots) return fail(PA_ERR_INVALID_ARG, "NULL input");
+    if (!aligned(nr.k, 16) || !aligned(nr.v, 16))
+        return fail(PA_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+    return PA_OK;
+}
+
 // Runs the planner, the split-KV kernel and the tensor-core kernel of one
 // step on `s`.  With `casc` (cascade decode, all rows short) the step is
 // the unique-suffix pass, run side by side with the shared-prefix pass.
@@ -865,11 +875,8 @@ int pa_write_kv(const void *k, const void *v, const int64_t *slot_mapping, int32
     g_err[0] = 0;
     int rc = check_kv(kv);
     if (rc != PA_OK) return rc;
-    if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
+    if ((rc = check_new_rows(NewRows{k, v, slot_mapping, num_tokens})) != PA_OK) return rc;
     if (num_tokens == 0) return PA_OK;
-    if (!k || !v || !slot_mapping) return fail(PA_ERR_INVALID_ARG, "NULL input");
-    if (!aligned(k, 16) || !aligned(v, 16))
-        return fail(PA_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
     DeviceInfo *dev;
     if ((rc = device_info(&dev)) != PA_OK) return rc;
     {
@@ -891,16 +898,6 @@ size_t pa_attention_workspace_size(int32_t num_seqs, int32_t num_q_tokens, int32
 }  // extern "C"
 
 namespace {
-
-// Checks of pa_write_kv's arguments; num_tokens == 0 needs no pointers.
-int check_new_rows(const NewRows &nr) {
-    if (nr.num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
-    if (nr.num_tokens == 0) return PA_OK;
-    if (!nr.k || !nr.v || !nr.slots) return fail(PA_ERR_INVALID_ARG, "NULL input");
-    if (!aligned(nr.k, 16) || !aligned(nr.v, 16))
-        return fail(PA_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
-    return PA_OK;
-}
 
 // pa_attention_ex, and with `fresh` the write of the step's new rows first.
 int attention_entry(const void *q, const pa_kv_desc *kv, const int32_t *block_tables,
