@@ -81,6 +81,26 @@ def test_write_kv_rejects_bad_arguments_on_host():
     assert pk.lib().pa_write_kv(f, f, f, 4, ctypes.byref(kv), None) == pk.PA_ERR_INVALID_ARG
 
 
+def call_fused(k=1 << 20, slots=1 << 20, n_new=4, head_dim=128, ws_bytes=1 << 30):
+    """pa_write_kv_attention with pointers that are never dereferenced: every
+    case below fails its host checks before any CUDA call."""
+    f = ctypes.c_void_p(1 << 20)
+    kv = pk.KVDesc(1 << 20, 1 << 21, 100, 16, 8, head_dim)
+    return pk.lib().pa_write_kv_attention(
+        ctypes.c_void_p(k), f, ctypes.c_void_p(slots) if slots else None, n_new, f,
+        ctypes.byref(kv), f, 4, f, f, f, 2, 3, 32, 0.1, f, None, ctypes.c_void_p(1 << 22),
+        ws_bytes, None)
+
+
+def test_write_kv_attention_rejects_bad_arguments_on_host():
+    assert call_fused(k=(1 << 20) + 8) == pk.PA_ERR_INVALID_ARG    # misaligned new K rows
+    assert call_fused(slots=0) == pk.PA_ERR_INVALID_ARG            # no slot mapping
+    assert call_fused(n_new=-1) == pk.PA_ERR_INVALID_ARG
+    assert call_fused(head_dim=96) == pk.PA_ERR_UNSUPPORTED
+    assert call_fused(ws_bytes=1024) == pk.PA_ERR_WORKSPACE
+    assert b"workspace" in pk.lib().pa_last_error_message()
+
+
 def good_meta():
     bt = torch.tensor([[3, 7, 11], [3, 7, 5]], dtype=torch.int32)
     qsl = torch.tensor([0, 5, 6], dtype=torch.int32)
